@@ -1,0 +1,91 @@
+"""Pins for the oracle's sequential protocol model.
+
+The model (oracle/protocol.py) runs the seq/parity slot protocol: Semaphore
+start/end barriers (common.cuh, ``PullController::sync``), the per-block
+parity epoch (common.cuh, ``PushController``), the zero-resetting signal pad
+(triton_barrier.py, ``blockwise_barrier``) and the last-block counters
+(arx.cu, ``arx_kernel``).  It is checked here against closed forms derived by
+hand from those definitions, and against the stated invariants of the pages:
+the pad is all zero after every completed barrier, ``counter == flag`` after
+an end stage, the epoch is the step count mod 2, and two slot banks hold the
+last two steps' inputs.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import protocol as P
+import synthetic_partials as sp
+
+M32 = 0xFFFFFFFF
+
+
+def _inputs(W, n, step):
+    return list(sp.to_u16_numpy(sp.partials(W, n, "normal", 4 + step)))
+
+
+@pytest.mark.parametrize("W,B,k", [(1, 1, 1), (2, 3, 2), (4, 2, 5), (8, 4, 7)])
+def test_closed_form_after_k_steps(W, B, k):
+    st = P.State(W=W, B=B)
+    hist = []
+    for s in range(k):
+        x = _inputs(W, 64, s)
+        hist.append(x)
+        out = P.step(st, x)
+        # Output is the rank-order reduce of this step's inputs.
+        assert np.array_equal(out, oracle.reduce(x))
+    # Each step adds W (start) + W (end) to every flag; the end stage moves the
+    # counter by 2W; so flag == counter == 2Wk.
+    assert (st.flag == 2 * W * k).all() and (st.counter == 2 * W * k).all()
+    assert (st.epoch == k % 2).all()
+    assert not st.pad.any()
+    assert st.blocks == [0, 0]
+    assert st.seq == k and st.published == k and st.err == 0
+    # Bank k & 1 holds step k's inputs, the other bank step k-1's.
+    for r in range(W):
+        assert np.array_equal(st.slots[k & 1][r], hist[k - 1][r])
+        if k >= 2:
+            assert np.array_equal(st.slots[(k - 1) & 1][r], hist[k - 2][r])
+
+
+def test_unsigned_wrap_of_seq_and_flags():
+    W, B = 8, 2
+    seq0 = M32 - 1          # two steps before seq wraps
+    flag0 = M32 - 5         # flags wrap during the first step
+    st = P.State(W=W, B=B, seq=seq0)
+    st.epoch[:] = seq0 % 2
+    st.flag[:] = flag0
+    st.counter[:] = flag0
+    for s in range(3):
+        P.step(st, _inputs(W, 16, s))
+    assert st.err == 0
+    assert st.seq == (seq0 + 3) & M32 == 1
+    assert (st.flag == (flag0 + 6 * W) & M32).all()
+    assert (st.counter == st.flag).all()
+    assert (st.epoch == (seq0 + 3) % 2).all()
+
+
+def test_missing_end_signal_reports_timeout():
+    st = P.State(W=4, B=2)
+    P.step(st, _inputs(4, 16, 0))
+    assert st.err == 0
+    P.step(st, _inputs(4, 16, 1), skip_end_signal_rank=2)
+    assert st.err == P.ETIMEOUT
+
+
+def test_epoch_mismatch_reports_state_error():
+    st = P.State(W=2, B=3)
+    st.epoch[1, 2] = 1
+    P.step(st, _inputs(2, 16, 0))
+    assert st.err == P.ESTATE
+
+
+def test_parity_alternates_banks():
+    st = P.State(W=2, B=1)
+    a, b, c = _inputs(2, 8, 0), _inputs(2, 8, 1), _inputs(2, 8, 2)
+    P.step(st, a)          # seq 1 -> bank 1
+    P.step(st, b)          # seq 2 -> bank 0
+    assert np.array_equal(st.slots[1][0], a[0]) and np.array_equal(st.slots[0][0], b[0])
+    P.step(st, c)          # seq 3 -> bank 1 again, bank 0 untouched
+    assert np.array_equal(st.slots[1][1], c[1]) and np.array_equal(st.slots[0][1], b[1])
