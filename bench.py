@@ -1,0 +1,498 @@
+"""Benchmark of the deterministic W-way bf16 reduce on GB300.
+
+Default workload: W = 8 bf16 partials of [32, 4096] (n = 131,072 elements,
+256 KiB each; normal(0, 1), seed 1) -- the decode-sized message of the
+one-shot all-reduce.  One step = one ``arx_reduce`` call: every element of
+the 8 partials is read once, summed in fp32 in rank order and written once
+as bf16.  Metric: HBM GB/s = (W + 1) * n * 2 bytes / time per call, and
+microseconds per call.
+
+Timing rules followed:
+* inputs resident in HBM before the timed region; the calls rotate over
+  enough buffer sets that their footprint is more than 3x the L2, so no call
+  finds its inputs in L2 (stated in ``config``);
+* >= 3 untimed warm-up steps, then exactly K timed steps, all launched from
+  CUDA graphs (captured off the clock) on one stream and bracketed by CUDA
+  events recorded on that stream, with a barrier and a device synchronise on
+  both sides; the maximum over ranks is reported;
+* nvidia-smi clocks and throttle reasons are sampled around the timed region.
+
+Extra objects on the one JSON line: ``roofline`` (the reduce kernel against
+the measured HBM copy bandwidth), ``cpu_baseline`` (the CPU oracle on the
+host's cores, a bounded sample), ``e2e`` (the same metric through
+``arx_reduce_host`` with pinned host buffers, copies included),
+``bandwidth`` (bandwidth-bound sizes: W=4 [1024, 8192] in place, W=8 at
+16 MiB and 256 MiB per partial), ``protocol`` (``arx_step`` per step in a
+captured graph).
+
+``--impl reference`` times the CPU oracle instead (the reference arm: there
+is no reference implementation to install, the pages hold no code to build).
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the reduce has no cross-GPU step on one box); value = all ranks'
+bytes / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W-way bf16 reduce HBM GB/s ((W+1)·n·2 B / t); µs/call at bf16 [32,4096]"
+DEFAULT_WORKLOAD = "w8_32x4096_normal"
+FALLBACK_HBM_GBS = 6800.0
+GRAPH_CALLS = 1000
+ROTATE_FACTOR = 3          # rotation footprint >= this many L2 sizes
+
+
+# ---------------------------------------------------------------------------------------------
+# host-side helpers (no GPU needed; covered by the gloo tests)
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate_over_ranks(elapsed_s: float, units: float) -> tuple[float, float]:
+    """(max elapsed over ranks, sum of units over ranks); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return elapsed_s, units
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier() -> None:
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def rotation_sets(set_bytes: int, l2_bytes: int, cap: int = 4096) -> int:
+    """Buffer sets needed so that the rotation footprint exceeds ROTATE_FACTOR x L2."""
+    need = (ROTATE_FACTOR * l2_bytes) // max(1, set_bytes) + 1
+    return int(max(1, min(cap, need)))
+
+
+def gbs(bytes_per_call: float, seconds_per_call: float) -> float:
+    return bytes_per_call / seconds_per_call / 1e9
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh)
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the reduce kernel's sources: ties a stored ncu traffic figure to this code."""
+    h = hashlib.sha256()
+    for rel in ("deterministic_shot_all_gb300/csrc/reduce.cu",
+                "deterministic_shot_all_gb300/csrc/arx_device.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (index, SM MHz, max, reasons)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]),
+                                 power=float(parts[4]) if parts[4][:1].isdigit() else None,
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        window = [r for r in rows if self.t0 is not None and self.t0 - 0.15 <= r["ts"] <= (self.t1 or 0) + 0.15]
+        used = window if window else rows
+        reasons = set()
+        for r in used:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in used),
+                "sm_max_mhz": max(r["smax"] for r in used),
+                "reasons": sorted(reasons),
+                "samples_in_window": len(window), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline object)
+
+def time_oracle(W: int, n_sample: int, calls: int | None, budget_s: float, threads: int,
+                seed: int = 1, dist: str = "normal") -> dict:
+    """Times the oracle over ``n_sample`` elements drawn like the workload's partials."""
+    import oracle
+    import synthetic_partials as sp
+    x = sp.partials(W, n_sample, dist, seed)
+    u = sp.to_u16_numpy(x)
+    slots = list(u)
+    out = oracle.reduce(slots, threads=threads)  # warm
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.reduce(slots, out=out, threads=threads)
+        done += 1
+        el = time.perf_counter() - t0
+        if (calls is not None and done >= calls) or (calls is None and el >= budget_s):
+            break
+    el = time.perf_counter() - t0
+    byts = (W + 1) * n_sample * 2 * done
+    return dict(calls=done, seconds=el, bytes=byts, gbs=byts / el / 1e9, threads=threads)
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synthetic_partials as sp
+    spec = sp.WORKLOADS[args.workload]
+    W, n = spec["W"], spec["n"] or args.n
+    threads = oracle.default_threads()
+    # Bound the whole run to about two minutes of host time: each step reduces
+    # a contiguous sample of the workload's elements.
+    per_elem_s = 2.0e-9 * W / max(1, threads) + 1e-10
+    budget = 120.0
+    n_step = int(max(4096, min(n, budget / max(1, args.steps + args.warmup) / per_elem_s)))
+    n_step = min(n, n_step)
+    time_oracle(W, n_step, args.warmup, 0.0, threads, spec["seed"], spec["dist"])
+    r = time_oracle(W, n_step, args.steps, 0.0, threads, spec["seed"], spec["dist"])
+    value = r["gbs"]
+    sample = (f"{args.steps} oracle calls, each over the first {n_step} of {n} elements of the "
+              f"{args.workload} partials (W={W}), {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds"] / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "W": W, "n": n, "n_per_step": n_step},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+
+def _graph_of_calls(torch, stream, fn, count):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(count):
+            fn(i)
+    return g
+
+
+def timed_graph_calls(torch, stream, fn, steps: int, warmup: int, chunk: int = GRAPH_CALLS,
+                      sampler: ClockSampler | None = None) -> float:
+    """Seconds for exactly ``steps`` calls of fn(i), launched from CUDA graphs on ``stream``."""
+    chunk = max(1, min(chunk, steps))
+    with torch.cuda.stream(stream):
+        for i in range(max(1, min(warmup, 8))):   # eager warm-up (launch caches, lazy init)
+            fn(i)
+    torch.cuda.synchronize()
+    g_full = _graph_of_calls(torch, stream, fn, chunk)
+    rem = steps % chunk
+    g_rem = _graph_of_calls(torch, stream, lambda i: fn(steps - rem + i), rem) if rem else None
+    # Warm-up replays (untimed): at least `warmup` calls.
+    for _ in range(max(1, (warmup + chunk - 1) // chunk)):
+        g_full.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    start.record(stream)
+    for _ in range(steps // chunk):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_native(args) -> None:
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import deterministic_shot_all_gb300 as arx
+    import synthetic_partials as sp
+
+    spec = sp.WORKLOADS[args.workload]
+    W, n = spec["W"], spec["n"] or args.n
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    bytes_call = (W + 1) * n * 2
+    stream = torch.cuda.Stream(device=dev)
+
+    # Inputs: the workload's partials, copied into R rotation sets (+ outputs).
+    x, alias = sp.workload(args.workload, n=n)
+    xd = x.to(dev)
+    set_bytes = W * n * 2 + (0 if alias else n * 2)
+    R = rotation_sets(set_bytes, l2)
+    parts = torch.empty(R, W, n, dtype=torch.bfloat16, device=dev)
+    parts.copy_(xd.unsqueeze(0).expand(R, W, n))
+    outs = parts[:, 0] if alias else torch.empty(R, n, dtype=torch.bfloat16, device=dev)
+    slot_lists = [[parts[k, r] for r in range(W)] for k in range(R)]
+
+    def call(i):
+        k = i % R
+        arx.arx_reduce(slot_lists[k], outs[k], stream=stream)
+
+    # Correctness of what is timed: one call checked bit for bit against the oracle.
+    if rank == 0 and not args.no_check:
+        import oracle
+        want = oracle.reduce(list(sp.to_u16_numpy(x)))
+        with torch.cuda.stream(stream):
+            call(0)
+        torch.cuda.synchronize()
+        got = sp.to_u16_numpy(outs[0].cpu())
+        if not (got == want).all():
+            raise SystemExit("bench: GPU output differs from the oracle; refusing to time it")
+        parts[0].copy_(xd)
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    t = timed_graph_calls(torch, stream, call, args.steps, args.warmup, sampler=sampler)
+    clocks = sampler.stop() if sampler else None
+    t_max, total_bytes = aggregate_over_ranks(t, bytes_call * args.steps)
+    value = total_bytes / t_max / 1e9
+    per_call = t / args.steps
+
+    extra = {}
+    if not args.quick:
+        extra["bandwidth"] = bandwidth_points(torch, arx, sp, dev, stream, l2)
+        extra["protocol"] = protocol_point(torch, arx, sp, dev, stream, l2, args.workload)
+        extra["e2e"] = e2e_point(torch, arx, sp, dev, stream, args.workload, max(200, min(args.steps, 2000)))
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_note = "of measured" if peak else "of fallback"
+    peak = float(peak) if peak else FALLBACK_HBM_GBS
+    achieved = gbs(bytes_call, per_call)
+    traffic = stored_traffic(args.workload)
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        r = time_oracle(W, n, None, args.cpu_seconds, threads, spec["seed"], spec["dist"])
+        cpu = {"value": r["gbs"], "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{r['calls']} full calls of the {args.workload} workload "
+                         f"(W={W}, n={n}) in {r['seconds']:.1f} s on {threads} host threads"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
+        "us_per_call": per_call * 1e6, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "W": W, "n": n, "shape": [32, 4096] if n == 32 * 4096 else [n],
+                   "out_aliases_slot0": alias, "l2": f"inputs rotate over {R} buffer sets "
+                   f"({R * set_bytes / 1e6:.0f} MB > {ROTATE_FACTOR}x L2 {l2 / 1e6:.0f} MB)",
+                   "launch": f"CUDA graphs of {min(GRAPH_CALLS, args.steps)} arx_reduce calls, replayed",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic,
+                     "kernel": f"reduce_vec_kernel<{W}>", "algorithmic_bytes_per_launch": bytes_call},
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def bandwidth_points(torch, arx, sp, dev, stream, l2) -> list:
+    """GB/s at bandwidth-bound sizes, same timing method (rotation > 3x L2, graphs)."""
+    pts = []
+    peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+    for name, W, n, alias in (("w4_1024x8192_alias", 4, 1024 * 8192, True),
+                              ("w8_sweep_int", 8, 1 << 23, False),
+                              ("w8_sweep_int", 8, 1 << 27, False)):
+        set_bytes = W * n * 2 + (0 if alias else n * 2)
+        R = rotation_sets(set_bytes, l2, cap=64)
+        # Timing only (parity at these sizes is in the tests): values drawn on the
+        # device with the workload's distribution, to keep host time short.
+        gen = torch.Generator(device=dev).manual_seed(3)
+        if name == "w8_sweep_int":
+            parts = torch.randint(-8, 9, (R, W, n), generator=gen, device=dev).to(torch.bfloat16)
+        else:
+            parts = (torch.randn((R, W, n), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+        outs = parts[:, 0] if alias else torch.empty(R, n, dtype=torch.bfloat16, device=dev)
+        slot_lists = [[parts[k, r] for r in range(W)] for k in range(R)]
+        calls = 200 if n <= (1 << 23) else 40
+
+        def call(i, slot_lists=slot_lists, outs=outs, R=R):
+            arx.arx_reduce(slot_lists[i % R], outs[i % R], stream=stream)
+
+        t = timed_graph_calls(torch, stream, call, calls, 5, chunk=calls)
+        b = (W + 1) * n * 2
+        g = gbs(b, t / calls)
+        pts.append({"workload": name, "W": W, "n": n, "partial_MiB": n * 2 / 2**20, "in_place": alias,
+                    "us_per_call": t / calls * 1e6, "GBs": g, "frac": g / peak, "rotation_sets": R})
+        del parts, outs, slot_lists
+        torch.cuda.empty_cache()
+    return pts
+
+
+def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:
+    """arx_step per step (W=8, [32,4096]) in captured graphs, fresh input sets rotating."""
+    W, n = 8, sp.N_32x4096
+    x, _ = sp.workload(workload)
+    R = rotation_sets(W * n * 2 * 2, l2)
+    parts = torch.empty(R, W, n, dtype=torch.bfloat16, device=dev)
+    parts.copy_(x.to(dev).unsqueeze(0).expand(R, W, n))
+    outs = torch.empty(R, n, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
+    ctx = arx.arx_ctx_init(ws, W, n)
+    lists = [[parts[k, r] for r in range(W)] for k in range(R)]
+
+    def call(i):
+        arx.arx_step(ctx, lists[i % R], outs[i % R], stream=stream)
+
+    steps = 2000
+    t = timed_graph_calls(torch, stream, call, steps, 10)
+    st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
+    return {"W": W, "n": n, "blocks_per_rank": ctx.nblocks, "steps": steps,
+            "us_per_step": t / steps * 1e6, "status": arx.arx_status_string(st), "seq": seq,
+            "reduce_model_GBs": gbs((W + 1) * n * 2, t / steps)}
+
+
+def e2e_point(torch, arx, sp, dev, stream, workload, steps) -> dict:
+    """The metric through arx_reduce_host: pinned host partials in, host result out, per step."""
+    x, _ = sp.workload(workload)
+    W, n = x.shape
+    host = [x[r].clone().pin_memory() for r in range(W)]
+    hout = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    staging = torch.empty(arx.arx_reduce_host_staging_bytes(W, n), dtype=torch.uint8, device=dev)
+
+    def call(i):
+        arx.arx_reduce_host(host, hout, staging, stream=stream)
+
+    t = timed_graph_calls(torch, stream, call, steps, 5, chunk=min(steps, 200))
+    return {"value": gbs((W + 1) * n * 2, t / steps), "unit": "GB/s",
+            "us_per_call": t / steps * 1e6, "steps": steps,
+            "h2d_bytes_per_step": W * n * 2, "d2h_bytes_per_step": n * 2,
+            "path": "arx_reduce_host: W cudaMemcpyAsync from pinned host, reduce, 1 copy back"}
+
+
+def main(argv=None) -> None:
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200000)
+    p.add_argument("--warmup", type=int, default=1000)
+    p.add_argument("--impl", choices=("native", "reference"), default="native")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   choices=["w2_32x4096_uniform", "w8_32x4096_normal", "w4_1024x8192_alias", "w8_sweep_int"])
+    p.add_argument("--n", type=int, default=1 << 23, help="elements per partial for w8_sweep_int")
+    p.add_argument("--quick", action="store_true", help="headline only (no bandwidth/protocol/e2e)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-check", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.steps < 1:
+        p.error("--steps must be >= 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

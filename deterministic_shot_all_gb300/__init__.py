@@ -1,0 +1,215 @@
+"""Deterministic W-way bf16 reduce for one GB300 (sm_103a): Python binding.
+
+This module only marshals arguments to the C ABI of ``libarx.so`` (declared
+in ``include/arx.h``): tensors become device pointers, the current torch
+stream becomes a ``cudaStream_t``.  Every step of the computation runs in the
+library's CUDA kernels.  Importing fails loudly when the library has not been
+built (``python -c "import __graft_entry__ as g; g.build()"``); there is no
+CPU fallback.
+
+Functions keep the C names:
+
+* ``arx_reduce(slots, out)``: out = bf16(rank-order fp32 sum of slots), out
+  may be one of the slots.
+* ``arx_reduce_host(host_slots, host_out, staging)``: the same from and to
+  host buffers, copies included.
+* ``arx_ctx_workspace_bytes / arx_ctx_init / arx_step / arx_ctx_query /
+  arx_ctx_reset / arx_ctx_set_timeout / arx_ctx_set_fault``: the seq/parity
+  protocol step with Semaphore epochs and a zero-resetting signal pad.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libarx.so")
+
+ARX_OK, ARX_EINVAL, ARX_EOVERLAP, ARX_ECUDA, ARX_ETIMEOUT, ARX_ESTATE = range(6)
+ARX_MAX_W = 8
+ARX_STEP_MAX_BLOCKS = 256
+ARX_DEFAULT_TIMEOUT_NS = 1_000_000_000
+
+
+class ArxError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{arx_status_string(status)}: {detail}" if detail else arx_status_string(status))
+        self.status = status
+
+
+class arx_ctx(ctypes.Structure):
+    """Mirror of ``struct arx_ctx`` in include/arx.h."""
+    _fields_ = [
+        ("magic", ctypes.c_uint32),
+        ("W", ctypes.c_int32),
+        ("nblocks", ctypes.c_int32),
+        ("fault_rank", ctypes.c_int32),
+        ("max_n", ctypes.c_uint64),
+        ("slot_stride", ctypes.c_uint64),
+        ("timeout_ns", ctypes.c_uint64),
+        ("ws", ctypes.c_void_p),
+        ("ws_bytes", ctypes.c_uint64),
+        ("off_epoch", ctypes.c_uint64),
+        ("off_sem", ctypes.c_uint64),
+        ("off_pad", ctypes.c_uint64),
+        ("off_slots", ctypes.c_uint64),
+        ("ctrl_bytes", ctypes.c_uint64),
+    ]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()'); there is no CPU fallback")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, u32p, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_uint64
+    ptrs = ctypes.POINTER(ctypes.c_void_p)
+    ctxp = ctypes.POINTER(arx_ctx)
+    sigs = {
+        "arx_status_string": ([i32], ctypes.c_char_p),
+        "arx_last_error": ([], ctypes.c_char_p),
+        "arx_reduce": ([ptrs, i32, vp, sz, vp], i32),
+        "arx_reduce_host_staging_bytes": ([i32, sz], sz),
+        "arx_reduce_host": ([ptrs, i32, vp, sz, vp, sz, vp], i32),
+        "arx_ctx_workspace_bytes": ([i32, sz, i32], sz),
+        "arx_ctx_init": ([ctxp, vp, sz, i32, sz, i32], i32),
+        "arx_ctx_set_timeout": ([ctxp, u64], i32),
+        "arx_ctx_set_fault": ([ctxp, i32], i32),
+        "arx_ctx_reset": ([ctxp, vp], i32),
+        "arx_step": ([ctxp, ptrs, vp, sz, vp], i32),
+        "arx_ctx_query": ([ctxp, u32p, u32p, vp], i32),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
+lib = _load()
+
+
+def arx_status_string(status: int) -> str:
+    return lib.arx_status_string(int(status)).decode()
+
+
+def arx_last_error() -> str:
+    return lib.arx_last_error().decode()
+
+
+def _check(status: int) -> None:
+    if status != ARX_OK:
+        raise ArxError(status, arx_last_error())
+
+
+def _ptr(x) -> int:
+    """Address of a tensor's first element, or an int address as given."""
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor or an integer address, got {type(x).__name__}")
+
+
+def _ptr_array(xs: Sequence) -> ctypes.Array:
+    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _numel(n, out) -> int:
+    if n is not None:
+        return int(n)
+    if hasattr(out, "numel"):
+        return int(out.numel())
+    raise ValueError("n is required when out is an address")
+
+
+def arx_reduce(slots: Sequence, out, n: int | None = None, stream=None, check: bool = True) -> int:
+    """Enqueue out = bf16(sum over slots in rank order, fp32) on ``stream``.
+
+    ``slots``: W (1..8) bf16 device tensors or addresses; ``out``: bf16 device
+    tensor or address, may be one of the slots.  Returns the arx_status (and
+    raises ArxError on failure when ``check``).
+    """
+    st = lib.arx_reduce(_ptr_array(slots), len(slots), _ptr(out), _numel(n, out), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_reduce_host_staging_bytes(W: int, n: int) -> int:
+    return int(lib.arx_reduce_host_staging_bytes(W, n))
+
+
+def arx_reduce_host(host_slots: Sequence, host_out, staging, n: int | None = None,
+                    stream=None, check: bool = True) -> int:
+    """Enqueue copy-in, reduce and copy-out for host (ideally pinned) buffers."""
+    nb = staging.numel() * staging.element_size() if hasattr(staging, "numel") else None
+    if nb is None:
+        raise TypeError("staging must be a device tensor")
+    st = lib.arx_reduce_host(_ptr_array(host_slots), len(host_slots), _ptr(host_out),
+                             _numel(n, host_out), _ptr(staging), nb, _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_ctx_workspace_bytes(W: int, max_n: int, nblocks: int = 0) -> int:
+    return int(lib.arx_ctx_workspace_bytes(W, max_n, nblocks))
+
+
+def arx_ctx_init(ws, W: int, max_n: int, nblocks: int = 0, ws_bytes: int | None = None) -> arx_ctx:
+    """Context for the protocol step over a zero-filled device workspace ``ws``."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size()
+    ctx = arx_ctx()
+    _check(lib.arx_ctx_init(ctypes.byref(ctx), _ptr(ws), ws_bytes, W, max_n, nblocks))
+    ctx._ws_ref = ws  # keep the workspace alive as long as the context
+    return ctx
+
+
+def arx_ctx_set_timeout(ctx: arx_ctx, ns: int) -> None:
+    _check(lib.arx_ctx_set_timeout(ctypes.byref(ctx), int(ns)))
+
+
+def arx_ctx_set_fault(ctx: arx_ctx, rank: int) -> None:
+    _check(lib.arx_ctx_set_fault(ctypes.byref(ctx), int(rank)))
+
+
+def arx_ctx_reset(ctx: arx_ctx, stream=None) -> None:
+    _check(lib.arx_ctx_reset(ctypes.byref(ctx), _stream(stream)))
+
+
+def arx_step(ctx: arx_ctx, inputs: Sequence, out, n: int | None = None, stream=None,
+             check: bool = True) -> int:
+    """Enqueue one protocol step: out = rank-order reduce of ``inputs``."""
+    st = lib.arx_step(ctypes.byref(ctx), _ptr_array(inputs), _ptr(out), _numel(n, out), _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_ctx_query(ctx: arx_ctx, stream=None) -> tuple[int, int, int]:
+    """Synchronise ``stream``; return (status, completed seq, device error word)."""
+    seq = ctypes.c_uint32(0)
+    err = ctypes.c_uint32(0)
+    st = lib.arx_ctx_query(ctypes.byref(ctx), ctypes.byref(seq), ctypes.byref(err), _stream(stream))
+    return st, seq.value, err.value
+
+
+__all__ = [
+    "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce",
+    "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
+    "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_reset", "arx_step", "arx_ctx_query",
+]

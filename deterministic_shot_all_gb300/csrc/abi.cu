@@ -1,0 +1,313 @@
+// C ABI of libarx: argument checks on the host, then kernel launches.
+//
+// Mirrors the checks of arx.cu's `arx_allreduce` (bf16, contiguous, equal
+// sizes, world size bounds) as status codes instead of exceptions or exit(),
+// and drops its 512 KB / multiple-of-8 limits.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "arx.h"
+#include "arx_internal.h"
+
+namespace {
+
+constexpr uint32_t kCtxMagic = 0x41525843u;  // "ARXC"
+constexpr size_t kHeaderBytes = 256;
+
+thread_local char g_last_error[256];
+
+arx_status fail(arx_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+arx_status fail_cuda(cudaError_t e, const char* what) {
+  return fail(ARX_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+arx_status ok() {
+  g_last_error[0] = '\0';
+  return ARX_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// [p, p + bytes) and [q, q + bytes): 0 disjoint, 1 identical, 2 partial overlap.
+int overlap_kind(const void* p, const void* q, size_t pbytes, size_t qbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + pbytes;
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + qbytes;
+  if (a1 <= b0 || b1 <= a0) return 0;
+  if (a0 == b0 && pbytes == qbytes) return 1;
+  return 2;
+}
+
+// Common checks of the W input pointers and the output.
+arx_status check_io(const void* const* in, int W, const void* out, size_t n, bool* out_alias) {
+  if (W < 1 || W > ARX_MAX_W) return fail(ARX_EINVAL, "W=%d outside 1..%d", W, ARX_MAX_W);
+  if (!in) return fail(ARX_EINVAL, "null pointer array");
+  if (!out) return fail(ARX_EINVAL, "null output pointer");
+  if (reinterpret_cast<uintptr_t>(out) & 1u) return fail(ARX_EINVAL, "output not 2-byte aligned");
+  if (n > (SIZE_MAX / 2) / 2) return fail(ARX_EINVAL, "n=%zu too large", n);
+  const size_t bytes = n * 2;
+  *out_alias = false;
+  for (int r = 0; r < W; ++r) {
+    if (!in[r]) return fail(ARX_EINVAL, "null input pointer %d", r);
+    if (reinterpret_cast<uintptr_t>(in[r]) & 1u) return fail(ARX_EINVAL, "input %d not 2-byte aligned", r);
+    const int k = overlap_kind(out, in[r], bytes, bytes);
+    if (k == 2) return fail(ARX_EOVERLAP, "output partially overlaps input %d", r);
+    if (k == 1) *out_alias = true;
+  }
+  return ARX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* arx_status_string(arx_status s) {
+  switch (s) {
+    case ARX_OK: return "ARX_OK";
+    case ARX_EINVAL: return "ARX_EINVAL: invalid argument";
+    case ARX_EOVERLAP: return "ARX_EOVERLAP: output partially overlaps an input";
+    case ARX_ECUDA: return "ARX_ECUDA: CUDA error";
+    case ARX_ETIMEOUT: return "ARX_ETIMEOUT: a bounded device wait expired";
+    case ARX_ESTATE: return "ARX_ESTATE: inconsistent protocol state";
+  }
+  return "ARX_?: unknown status";
+}
+
+const char* arx_last_error(void) { return g_last_error; }
+
+arx_status arx_reduce(const void* const* slots, int W, void* out, size_t n, void* stream) {
+  if (n == 0) return ok();
+  bool alias = false;
+  const arx_status s = check_io(slots, W, out, n, &alias);
+  if (s != ARX_OK) return s;
+  arx::ReduceCall c{};
+  for (int r = 0; r < W; ++r) c.slot[r] = static_cast<const uint16_t*>(slots[r]);
+  c.out = static_cast<uint16_t*>(out);
+  c.n = n;
+  c.W = W;
+  c.out_aliases_slot = alias;
+  const cudaError_t e = arx::launch_reduce(c, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "arx_reduce launch");
+  return ok();
+}
+
+size_t arx_reduce_host_staging_bytes(int W, size_t n) {
+  if (W < 1 || W > ARX_MAX_W || n > (SIZE_MAX / 4) / ARX_MAX_W) return 0;
+  return size_t(W) * round_up(n * 2, 256);
+}
+
+arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out, size_t n,
+                           void* dev_staging, size_t staging_bytes, void* stream) {
+  if (n == 0) return ok();
+  if (W < 1 || W > ARX_MAX_W) return fail(ARX_EINVAL, "W=%d outside 1..%d", W, ARX_MAX_W);
+  if (!host_slots || !host_out) return fail(ARX_EINVAL, "null host pointer");
+  for (int r = 0; r < W; ++r)
+    if (!host_slots[r]) return fail(ARX_EINVAL, "null host slot %d", r);
+  if (!dev_staging) return fail(ARX_EINVAL, "null staging buffer");
+  if (reinterpret_cast<uintptr_t>(dev_staging) & 1u) return fail(ARX_EINVAL, "staging not 2-byte aligned");
+  const size_t need = arx_reduce_host_staging_bytes(W, n);
+  if (need == 0 || staging_bytes < need)
+    return fail(ARX_EINVAL, "staging buffer %zu bytes, need %zu", staging_bytes, need);
+  const size_t stride = round_up(n * 2, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(dev_staging);
+  const void* dev_slots[ARX_MAX_W];
+  for (int r = 0; r < W; ++r) {
+    dev_slots[r] = base + size_t(r) * stride;
+    const cudaError_t e = cudaMemcpyAsync(base + size_t(r) * stride, host_slots[r], n * 2,
+                                          cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return fail_cuda(e, "arx_reduce_host copy in");
+  }
+  arx::ReduceCall c{};
+  for (int r = 0; r < W; ++r) c.slot[r] = static_cast<const uint16_t*>(dev_slots[r]);
+  c.out = reinterpret_cast<uint16_t*>(base);  // in place over staged slot 0
+  c.n = n;
+  c.W = W;
+  c.out_aliases_slot = true;
+  cudaError_t e = arx::launch_reduce(c, st);
+  if (e != cudaSuccess) return fail_cuda(e, "arx_reduce_host launch");
+  e = cudaMemcpyAsync(host_out, base, n * 2, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail_cuda(e, "arx_reduce_host copy out");
+  return ok();
+}
+
+// ---- protocol context ----------------------------------------------------------
+
+namespace {
+
+struct Layout {
+  size_t off_epoch, off_sem, off_pad, off_slots, slot_stride, total;
+};
+
+bool layout(int W, size_t max_n, int B, Layout* L) {
+  if (W < 1 || W > ARX_MAX_W || B < 1 || B > ARX_STEP_MAX_BLOCKS) return false;
+  if (max_n > (SIZE_MAX / 8) / (2 * ARX_MAX_W)) return false;
+  L->off_epoch = kHeaderBytes;
+  L->off_sem = round_up(L->off_epoch + size_t(W) * B * 4, 128);
+  L->off_pad = round_up(L->off_sem + size_t(W) * B * 128, 128);
+  L->off_slots = round_up(L->off_pad + size_t(W) * B * W * 4, 256);
+  L->slot_stride = round_up(max_n > 0 ? max_n : 1, 128);  // elements; 256-byte multiple
+  L->total = L->off_slots + 2 * size_t(W) * L->slot_stride * 2;
+  return true;
+}
+
+int auto_blocks(int W, size_t max_n, arx_status* s) {
+  cudaError_t e = cudaSuccess;
+  const int sms = arx::current_sm_count(&e);
+  if (sms < 1) {
+    *s = fail_cuda(e, "arx_ctx_init device query");
+    return -1;
+  }
+  const int cap = arx::step_capacity(W, &e);
+  if (cap < 1) {
+    *s = fail_cuda(e, "arx_ctx_init occupancy query");
+    return -1;
+  }
+  // About one block per SM over the W*B grid, at least 32 groups of 8
+  // elements per reducing block, within the resident capacity.
+  size_t B = size_t(sms) / size_t(W);
+  const size_t groups = (max_n + 7) / 8;
+  const size_t by_work = (groups + size_t(W) * 32 - 1) / (size_t(W) * 32);
+  if (B > by_work) B = by_work;
+  if (B > size_t(cap / W)) B = size_t(cap / W);
+  if (B > ARX_STEP_MAX_BLOCKS) B = ARX_STEP_MAX_BLOCKS;
+  if (B < 1) B = 1;
+  *s = ARX_OK;
+  return int(B);
+}
+
+arx_status check_ctx(const arx_ctx* ctx) {
+  if (!ctx || ctx->magic != kCtxMagic) return fail(ARX_ESTATE, "context not initialised");
+  return ARX_OK;
+}
+
+}  // namespace
+
+size_t arx_ctx_workspace_bytes(int W, size_t max_n, int nblocks) {
+  Layout L;
+  if (!layout(W, max_n, nblocks == 0 ? ARX_STEP_MAX_BLOCKS : nblocks, &L)) return 0;
+  return L.total;
+}
+
+arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t max_n, int nblocks) {
+  if (!ctx) return fail(ARX_EINVAL, "null ctx");
+  std::memset(ctx, 0, sizeof *ctx);
+  if (W < 1 || W > ARX_MAX_W) return fail(ARX_EINVAL, "W=%d outside 1..%d", W, ARX_MAX_W);
+  if (nblocks < 0 || nblocks > ARX_STEP_MAX_BLOCKS)
+    return fail(ARX_EINVAL, "nblocks=%d outside 0..%d", nblocks, ARX_STEP_MAX_BLOCKS);
+  if (!ws) return fail(ARX_EINVAL, "null workspace");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(ARX_EINVAL, "workspace not 256-byte aligned");
+  int B = nblocks;
+  if (B == 0) {
+    arx_status s = ARX_OK;
+    B = auto_blocks(W, max_n, &s);
+    if (B < 1) return s;
+  }
+  Layout L;
+  if (!layout(W, max_n, B, &L)) return fail(ARX_EINVAL, "max_n=%zu too large", max_n);
+  if (ws_bytes < L.total) return fail(ARX_EINVAL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  ctx->magic = kCtxMagic;
+  ctx->W = W;
+  ctx->nblocks = B;
+  ctx->fault_rank = -1;
+  ctx->max_n = max_n;
+  ctx->slot_stride = L.slot_stride;
+  ctx->timeout_ns = ARX_DEFAULT_TIMEOUT_NS;
+  ctx->ws = ws;
+  ctx->ws_bytes = ws_bytes;
+  ctx->off_epoch = L.off_epoch;
+  ctx->off_sem = L.off_sem;
+  ctx->off_pad = L.off_pad;
+  ctx->off_slots = L.off_slots;
+  ctx->ctrl_bytes = L.off_slots;
+  return ok();
+}
+
+arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns) {
+  const arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  if (ns == 0) return fail(ARX_EINVAL, "timeout must be > 0");
+  ctx->timeout_ns = ns;
+  return ok();
+}
+
+arx_status arx_ctx_set_fault(arx_ctx* ctx, int rank) {
+  const arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  if (rank < -1 || rank >= ctx->W) return fail(ARX_EINVAL, "fault rank %d outside -1..%d", rank, ctx->W - 1);
+  ctx->fault_rank = rank;
+  return ok();
+}
+
+arx_status arx_ctx_reset(const arx_ctx* ctx, void* stream) {
+  const arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  const cudaError_t e = cudaMemsetAsync(ctx->ws, 0, ctx->ctrl_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "arx_ctx_reset");
+  return ok();
+}
+
+arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, size_t n, void* stream) {
+  arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  if (n == 0) return ok();
+  if (n > ctx->max_n) return fail(ARX_EINVAL, "n=%zu exceeds the context's max_n=%llu", n,
+                                  static_cast<unsigned long long>(ctx->max_n));
+  bool alias = false;
+  s = check_io(inputs, ctx->W, out, n, &alias);
+  if (s != ARX_OK) return s;
+  if (overlap_kind(out, ctx->ws, n * 2, ctx->ws_bytes) != 0)
+    return fail(ARX_EOVERLAP, "output overlaps the workspace");
+  cudaError_t e = cudaSuccess;
+  const int cap = arx::step_capacity(ctx->W, &e);
+  if (cap < 1) return fail_cuda(e, "arx_step occupancy query");
+  if (ctx->nblocks * ctx->W > cap)
+    return fail(ARX_EINVAL, "grid %d x %d exceeds the %d co-resident blocks of this device",
+                ctx->nblocks, ctx->W, cap);
+  arx::StepCall c{};
+  for (int r = 0; r < ctx->W; ++r) c.in[r] = static_cast<const uint16_t*>(inputs[r]);
+  c.out = static_cast<uint16_t*>(out);
+  c.n = n;
+  c.ws = static_cast<uint8_t*>(ctx->ws);
+  c.off_epoch = ctx->off_epoch;
+  c.off_sem = ctx->off_sem;
+  c.off_pad = ctx->off_pad;
+  c.off_slots = ctx->off_slots;
+  c.slot_stride = ctx->slot_stride;
+  c.timeout_ns = ctx->timeout_ns;
+  c.W = ctx->W;
+  c.B = ctx->nblocks;
+  c.fault_rank = ctx->fault_rank;
+  e = arx::launch_step(c, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "arx_step launch");
+  return ok();
+}
+
+arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream) {
+  const arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t words[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(words, ctx->ws, sizeof words, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail_cuda(e, "arx_ctx_query");
+  if (seq) *seq = words[0];
+  if (dev_err) *dev_err = words[1];
+  const uint32_t code = words[1] & 0xFFu;
+  if (code == 0) return ok();
+  if (code == ARX_ETIMEOUT || code == ARX_ESTATE)
+    return fail(static_cast<arx_status>(code), "device error word 0x%08x (stage %u, rank %u, block %u)",
+                words[1], (words[1] >> 8) & 15u, (words[1] >> 12) & 15u, words[1] >> 16);
+  return fail(ARX_ESTATE, "device error word 0x%08x", words[1]);
+}
+
+}  // extern "C"

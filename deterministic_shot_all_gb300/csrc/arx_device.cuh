@@ -1,0 +1,165 @@
+// Device helpers shared by the reduce and protocol kernels (sm_103a).
+//
+// Arithmetic of the reduce (arx.cu, `arx_kernel`, reduce loop): each bf16 is
+// widened to fp32 exactly (its 16 bits become the upper half of a binary32),
+// added into an fp32 accumulator that starts at +0 in rank order with
+// round-to-nearest-even adds (add.rn.f32: never contracted, never flushed --
+// the build passes no fast-math and keeps -ftz=false), and rounded once to
+// bf16 with cvt.rn (nearest, ties to even).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace arx {
+
+constexpr int kMaxW = 8;
+constexpr int kThreads = 256;
+
+// ---- bf16 <-> fp32 ------------------------------------------------------------
+
+// Low / high bf16 of a packed 32-bit word, widened exactly.
+__device__ __forceinline__ float widen_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float widen_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float widen16(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+
+// Two fp32 -> one word of two bf16 (lo in bits 0-15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ uint16_t round_bf16(float x) {
+  uint16_t d;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(d) : "f"(x));
+  return d;
+}
+
+// acc[0..7] += the 8 bf16 of one 16-byte vector (element k of the group in acc[k]).
+__device__ __forceinline__ void accumulate8(float (&acc)[8], const uint4& v) {
+  acc[0] = __fadd_rn(acc[0], widen_lo(v.x));
+  acc[1] = __fadd_rn(acc[1], widen_hi(v.x));
+  acc[2] = __fadd_rn(acc[2], widen_lo(v.y));
+  acc[3] = __fadd_rn(acc[3], widen_hi(v.y));
+  acc[4] = __fadd_rn(acc[4], widen_lo(v.z));
+  acc[5] = __fadd_rn(acc[5], widen_hi(v.z));
+  acc[6] = __fadd_rn(acc[6], widen_lo(v.w));
+  acc[7] = __fadd_rn(acc[7], widen_hi(v.w));
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  return o;
+}
+
+// Rank-order sum of W vectors: acc from +0, slot 0 first.
+template <int W>
+__device__ __forceinline__ uint4 sum_vectors(const uint4 (&v)[W]) {
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+#pragma unroll
+  for (int r = 0; r < W; ++r) accumulate8(acc, v[r]);
+  return pack8(acc);
+}
+
+// ---- 16-byte global loads and stores --------------------------------------------
+
+// Read-only streaming load: non-coherent path, no L1 allocation.  Only for
+// data no thread of the same kernel writes.
+__device__ __forceinline__ uint4 ld_stream_nc(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// Coherent streaming load (safe when the same kernel writes the location
+// after reading it, e.g. in-place output), no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+
+// Load cached at L2 only: for data other blocks of this kernel wrote before a
+// release/acquire handshake (never served from a stale L1 line).
+__device__ __forceinline__ uint4 ld_cg(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_cg16(const uint16_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_global(uint4* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// ---- scoped atomics and loads for the protocol words (one GPU: .gpu scope) -------
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t atom_cas_relaxed_gpu(uint32_t* p, uint32_t cmp, uint32_t val) {
+  uint32_t old;
+  asm volatile("atom.relaxed.gpu.global.cas.b32 %0, [%1], %2, %3;"
+               : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Spin budget that ends a wait even if the global timer stood still: every
+// poll is a round trip to L2 (hundreds of ns) and, after the first 1024 polls,
+// also sleeps, so timeout_ns / 64 polls last longer than timeout_ns.
+__device__ __forceinline__ uint64_t spin_cap(uint64_t timeout_ns) {
+  return 4096u + timeout_ns / 64u;
+}
+
+__device__ __forceinline__ void backoff(uint64_t spins) {
+  if (spins > 1024u) __nanosleep(128);
+}
+
+}  // namespace arx

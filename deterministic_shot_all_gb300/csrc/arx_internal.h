@@ -1,0 +1,45 @@
+// Host-side interface between the C ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace arx {
+
+// One stateless reduce: out[i] = bf16(sum_r slot[r][i]) for 0 <= i < n.
+struct ReduceCall {
+  const uint16_t* slot[8];
+  uint16_t* out;
+  size_t n;
+  int W;
+  bool out_aliases_slot;  // out equals one slot pointer
+};
+
+// Enqueues the reduce on `stream`.  Picks the vector kernel when every
+// pointer has the same address mod 16, else the scalar kernel.
+cudaError_t launch_reduce(const ReduceCall& c, cudaStream_t stream);
+
+// One protocol step (see arx.h, arx_step).
+struct StepCall {
+  const uint16_t* in[8];
+  uint16_t* out;
+  size_t n;
+  uint8_t* ws;
+  uint64_t off_epoch, off_sem, off_pad, off_slots, slot_stride;
+  uint64_t timeout_ns;
+  int W, B;
+  int fault_rank;
+};
+
+cudaError_t launch_step(const StepCall& c, cudaStream_t stream);
+
+// Most blocks of the step kernel for W ranks that can be resident at once on
+// the current device (SMs x blocks per SM), or a negative value on error.
+int step_capacity(int W, cudaError_t* err);
+
+// SM count of the current device (cached per device ordinal).
+int current_sm_count(cudaError_t* err);
+
+}  // namespace arx

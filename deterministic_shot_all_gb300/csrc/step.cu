@@ -1,0 +1,337 @@
+// One protocol step of the one-shot all-reduce, as a single kernel on one GPU.
+//
+// The pages run one kernel per rank on different GPUs and synchronise them
+// through flags.  Here the W ranks are W virtual ranks inside one grid of
+// B x W blocks: block (b, r) = (blockIdx.x, blockIdx.y) plays rank r's block b.
+//
+//  1. seq/parity (arx.cu, `arx_kernel`): seq = completed + 1, bank = seq & 1.
+//     The per-block parity epoch (common.cuh, `PushController`, two stages)
+//     must equal (seq - 1) & 1.
+//  2. start barrier (common.cuh, `PullController::sync`, start stage,
+//     unfenced): lane 0 of warp q < W adds 1 to Semaphore sem[q][b]; warp r
+//     waits until flag - counter >= W; then the block synchronises.
+//  3. stage: rank r's chunk b -> slots[bank][r] (stands in for the RDMA write
+//     into every peer's recv[seq & 1][rank]); the last block past the copy
+//     resets the first block counter and publishes seq (arx.cu "last block
+//     publishes").
+//  4. end barrier (`PullController::sync`, end stage, fenced): block barrier,
+//     release-add 1 to sem[q][b] for every q, warp r waits with acquire until
+//     flag - counter >= 2W and sets counter += 2W.
+//  5. reduce: sub-range r of chunk b over slots[bank][0..W-1] in rank order.
+//  6. exit: triton_barrier.py `blockwise_barrier`, Pattern 2 (relaxed):
+//     thread t < W sends pad[t][b][r] 0 -> 1 and waits pad[r][b][t] 1 -> 0, so
+//     the pad is all zero again; `PushController::exit` flips epoch[r][b];
+//     the last block out resets the second counter and stores seq as
+//     completed (arx.cu "last block out").
+//
+// Every wait is bounded by the context's timeout (global timer plus a spin
+// cap): on expiry the block records ARX_ETIMEOUT with its stage, rank and
+// block in the error word and carries on, so the kernel always finishes and
+// the host reads the status.  The pages' waits are unbounded; these are not.
+#include "arx_device.cuh"
+#include "arx_internal.h"
+
+namespace arx {
+namespace {
+
+// Status codes written to the device error word (same values as arx_status).
+constexpr uint32_t kErrTimeout = 4;
+constexpr uint32_t kErrState = 5;
+
+enum Stage : uint32_t { kStartWait = 1, kEndWait = 2, kPadSend = 3, kPadWait = 4, kEpoch = 5 };
+
+struct Header {  // first bytes of the workspace
+  uint32_t seq;        // completed steps
+  uint32_t err;        // device error word
+  uint32_t blocks[2];  // blocks past staging / blocks finished
+  uint32_t published;  // last staged seq
+};
+
+// common.cuh `Semaphore`: 128-byte aligned flag + counter; the counter is
+// read and written only by the owning block.
+struct alignas(128) Semaphore {
+  uint32_t flag;
+  uint32_t counter;
+};
+
+struct StepArgs {
+  const uint16_t* in[kMaxW];
+  uint16_t* out;
+  size_t n;
+  uint8_t* ws;
+  uint64_t off_epoch, off_sem, off_pad, off_slots, slot_stride;
+  uint64_t timeout_ns;
+  int B;
+  int fault_rank;
+  uint32_t in_vec_mask;  // bit r: input r is 16-byte aligned
+  int out_vec;           // out is 16-byte aligned
+};
+
+__device__ __forceinline__ void record_error(uint32_t* err, uint32_t code, uint32_t stage,
+                                             uint32_t r, uint32_t b) {
+  const uint32_t word = code | (stage << 8) | ((r & 15u) << 12) | ((b & 0xFFFFu) << 16);
+  atomicCAS(err, 0u, word);
+}
+
+// Wait until flag - base >= target (unsigned), bounded.  kFence selects an
+// acquire load (end stage) or a relaxed one (start stage).
+template <bool kFence>
+__device__ bool semaphore_wait(const uint32_t* flag, uint32_t base, uint32_t target,
+                               uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  const uint64_t cap = spin_cap(timeout_ns);
+  for (uint64_t spins = 0;; ++spins) {
+    const uint32_t v = kFence ? ld_acquire_gpu(flag) : ld_relaxed_gpu(flag);
+    if (v - base >= target) return true;
+    if ((spins & 15u) == 15u) {
+      if (global_timer_ns() - t0 > timeout_ns || spins > cap) return false;
+      backoff(spins);
+    }
+  }
+}
+
+// Compare-and-swap `from -> to` until it succeeds, bounded.
+__device__ bool cas_until(uint32_t* p, uint32_t from, uint32_t to, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  const uint64_t cap = spin_cap(timeout_ns);
+  for (uint64_t spins = 0;; ++spins) {
+    if (atom_cas_relaxed_gpu(p, from, to) == from) return true;
+    if ((spins & 15u) == 15u) {
+      if (global_timer_ns() - t0 > timeout_ns || spins > cap) return false;
+      backoff(spins);
+    }
+  }
+}
+
+__device__ __forceinline__ size_t split_point(size_t total, uint32_t parts, uint32_t i) {
+  return total / parts * i + (total % parts) * i / parts;
+}
+
+template <int W>
+__global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
+  const uint32_t b = blockIdx.x, r = blockIdx.y;
+  const uint32_t B = uint32_t(a.B);
+  const uint32_t tid = threadIdx.x, warp = tid / 32u, lane = tid % 32u;
+  Header* hdr = reinterpret_cast<Header*>(a.ws);
+  uint32_t* epoch = reinterpret_cast<uint32_t*>(a.ws + a.off_epoch);
+  Semaphore* sem = reinterpret_cast<Semaphore*>(a.ws + a.off_sem);
+  uint32_t* pad = reinterpret_cast<uint32_t*>(a.ws + a.off_pad);
+  uint16_t* slots = reinterpret_cast<uint16_t*>(a.ws + a.off_slots);
+  const uint32_t total_blocks = B * uint32_t(W);
+
+  __shared__ uint32_t s_seq;
+
+  // 1. seq / parity; epoch check.
+  if (tid == 0) {
+    const uint32_t seq = ld_relaxed_gpu(&hdr->seq) + 1u;
+    s_seq = seq;
+    if (epoch[r * B + b] != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
+  }
+
+  // 2. start barrier, unfenced: no block barrier before the signal.
+  Semaphore& own = sem[r * B + b];
+  uint32_t base = 0;
+  if (lane == 0 && warp < uint32_t(W)) {
+    atom_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
+    if (warp == r) {
+      base = own.counter;
+      if (!semaphore_wait<false>(&own.flag, base, uint32_t(W), a.timeout_ns))
+        record_error(&hdr->err, kErrTimeout, kStartWait, r, b);
+    }
+  }
+  __syncthreads();
+  const uint32_t seq = s_seq;
+  const uint32_t par = seq & 1u;
+  const size_t stride = size_t(a.slot_stride);
+  uint16_t* bank = slots + size_t(par) * size_t(W) * stride;
+
+  // 3. stage rank r's chunk b into slots[par][r].
+  const size_t G = a.n / 8u;
+  const size_t tail = a.n - 8u * G;
+  const size_t c0 = split_point(G, B, b), c1 = split_point(G, B, b + 1u);
+  {
+    const uint16_t* in = a.in[r];
+    uint16_t* dst = bank + size_t(r) * stride;
+    if ((a.in_vec_mask >> r) & 1u) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(in);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      for (size_t g = c0 + tid; g < c1; g += kThreads) st_global(d4 + g, ld_stream(s4 + g));
+    } else {
+      for (size_t e = 8u * c0 + tid; e < 8u * c1; e += kThreads) dst[e] = in[e];
+    }
+    if (b == B - 1u && tid < tail) dst[8u * G + tid] = in[8u * G + tid];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {  // last block publishes
+      hdr->blocks[0] = 0u;
+      st_relaxed_gpu(&hdr->published, seq);
+    }
+  }
+
+  // 4. end barrier, fenced: every thread's staging precedes the release.
+  __syncthreads();
+  if (lane == 0 && warp < uint32_t(W)) {
+    if (int(r) != a.fault_rank) {
+      __threadfence();
+      atom_add_release_gpu(&sem[warp * B + b].flag, 1u);
+    }
+    if (warp == r) {
+      if (semaphore_wait<true>(&own.flag, base, 2u * uint32_t(W), a.timeout_ns)) {
+        __threadfence();
+        own.counter = base + 2u * uint32_t(W);
+      } else {
+        record_error(&hdr->err, kErrTimeout, kEndWait, r, b);
+      }
+    }
+  }
+  __syncthreads();
+
+  // 5. reduce sub-range r of chunk b over slots[par][0..W-1].
+  {
+    const size_t s0 = c0 + split_point(c1 - c0, uint32_t(W), r);
+    const size_t s1 = c0 + split_point(c1 - c0, uint32_t(W), r + 1u);
+    const uint4* src[W];
+#pragma unroll
+    for (int q = 0; q < W; ++q) src[q] = reinterpret_cast<const uint4*>(bank + size_t(q) * stride);
+    for (size_t g = s0 + tid; g < s1; g += kThreads) {
+      uint4 v[W];
+#pragma unroll
+      for (int q = 0; q < W; ++q) v[q] = ld_cg(src[q] + g);
+      const uint4 o = sum_vectors<W>(v);
+      if (a.out_vec) {
+        st_global(reinterpret_cast<uint4*>(a.out) + g, o);
+      } else {
+        uint16_t* d = a.out + 8u * g;
+        d[0] = uint16_t(o.x & 0xFFFFu);
+        d[1] = uint16_t(o.x >> 16);
+        d[2] = uint16_t(o.y & 0xFFFFu);
+        d[3] = uint16_t(o.y >> 16);
+        d[4] = uint16_t(o.z & 0xFFFFu);
+        d[5] = uint16_t(o.z >> 16);
+        d[6] = uint16_t(o.w & 0xFFFFu);
+        d[7] = uint16_t(o.w >> 16);
+      }
+    }
+    if (b == B - 1u && r == uint32_t(W) - 1u && tid < tail) {
+      const size_t e = 8u * G + tid;
+      float acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < W; ++q) acc = __fadd_rn(acc, widen16(ld_cg16(bank + size_t(q) * stride + e)));
+      a.out[e] = round_bf16(acc);
+    }
+  }
+
+  // 6. exit: zero-resetting pad barrier (Pattern 2: block barrier, then relaxed).
+  __syncthreads();
+  if (tid < uint32_t(W)) {
+    const uint32_t t = tid;
+    if (!cas_until(&pad[(t * B + b) * uint32_t(W) + r], 0u, 1u, a.timeout_ns))
+      record_error(&hdr->err, kErrTimeout, kPadSend, r, b);
+    if (!cas_until(&pad[(r * B + b) * uint32_t(W) + t], 1u, 0u, a.timeout_ns))
+      record_error(&hdr->err, kErrTimeout, kPadWait, r, b);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    epoch[r * B + b] = (epoch[r * B + b] + 1u) % 2u;  // PushController::exit
+    __threadfence();
+    if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
+      hdr->blocks[1] = 0u;
+      __threadfence();
+      st_relaxed_gpu(&hdr->seq, seq);
+    }
+  }
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int W>
+int blocks_per_sm(int dev, cudaError_t* err) {
+  static int cache[kMaxDevices];
+  if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  int b = 0;
+  *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, step_kernel<W>, kThreads, 0);
+  if (*err != cudaSuccess || b < 1) return -1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev] = b;
+  return b;
+}
+
+template <int W>
+cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
+  StepArgs a{};
+  for (int r = 0; r < W; ++r) a.in[r] = c.in[r];
+  a.out = c.out;
+  a.n = c.n;
+  a.ws = c.ws;
+  a.off_epoch = c.off_epoch;
+  a.off_sem = c.off_sem;
+  a.off_pad = c.off_pad;
+  a.off_slots = c.off_slots;
+  a.slot_stride = c.slot_stride;
+  a.timeout_ns = c.timeout_ns;
+  a.B = c.B;
+  a.fault_rank = c.fault_rank;
+  for (int r = 0; r < W; ++r)
+    if ((reinterpret_cast<uintptr_t>(c.in[r]) & 15u) == 0) a.in_vec_mask |= 1u << r;
+  a.out_vec = (reinterpret_cast<uintptr_t>(c.out) & 15u) == 0;
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(c.B), unsigned(W), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  // Every block of the grid waits on others: the launch must make them all
+  // resident at once.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, step_kernel<W>, a);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+template <int W>
+int capacity_w(cudaError_t* err) {
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return -1;
+  const int sms = current_sm_count(err);
+  if (sms < 1) return -1;
+  const int per = blocks_per_sm<W>(dev, err);
+  if (per < 1) return -1;
+  return sms * per;
+}
+
+}  // namespace
+
+cudaError_t launch_step(const StepCall& c, cudaStream_t stream) {
+  switch (c.W) {
+    case 1: return launch_w<1>(c, stream);
+    case 2: return launch_w<2>(c, stream);
+    case 3: return launch_w<3>(c, stream);
+    case 4: return launch_w<4>(c, stream);
+    case 5: return launch_w<5>(c, stream);
+    case 6: return launch_w<6>(c, stream);
+    case 7: return launch_w<7>(c, stream);
+    case 8: return launch_w<8>(c, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int step_capacity(int W, cudaError_t* err) {
+  switch (W) {
+    case 1: return capacity_w<1>(err);
+    case 2: return capacity_w<2>(err);
+    case 3: return capacity_w<3>(err);
+    case 4: return capacity_w<4>(err);
+    case 5: return capacity_w<5>(err);
+    case 6: return capacity_w<6>(err);
+    case 7: return capacity_w<7>(err);
+    case 8: return capacity_w<8>(err);
+    default: *err = cudaErrorInvalidValue; return -1;
+  }
+}
+
+}  // namespace arx

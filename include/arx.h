@@ -1,0 +1,205 @@
+/*
+ * arx.h -- C ABI of the deterministic W-way bf16 reduce on one GB300 (sm_103a).
+ *
+ * The operation is the data-parallel core of the one-shot all-reduce of
+ * arx.cu ("one-shot all-reduce over RoCE for GB10, no NCCL"): the sum of W
+ * bf16 partials, each element widened to fp32, accumulated from +0.0 in rank
+ * order 0, 1, ..., W-1, and rounded once to bf16 (round to nearest, ties to
+ * even), so that every consumer gets the same bits (arx.cu, `arx_kernel`,
+ * reduce loop, "rank order: every rank gets the same bits").  On one GPU the
+ * W rank partials are W slots in this GPU's HBM; there are no peers.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device (or managed) addresses of this
+ *    process's current device; pointers named "host" are host addresses.
+ *  - bf16 data is passed as untyped pointers to IEEE bfloat16 elements
+ *    (2 bytes, little-endian), contiguous, element i at byte offset 2*i.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Work is enqueued on it and the call returns without waiting,
+ *    except where a function says it synchronises.
+ *  - The library allocates no memory, holds no per-call state and owns no
+ *    buffer: the caller owns every byte (PyTorch tensors in the Python
+ *    binding).  Nothing here takes ownership of a pointer.
+ *  - Errors are returned as arx_status; nothing calls exit() or throws.
+ *    Argument errors are detected on the host before anything is enqueued.
+ *    arx_last_error() gives a one-line detail for the calling thread.
+ *  - Enqueuing entry points (arx_reduce, arx_step) launch kernels only, so
+ *    they can be captured into a CUDA graph (arx.cu: allreduce "runs on the
+ *    current stream and is CUDA-graph capturable").
+ */
+#ifndef ARX_H_
+#define ARX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Most ranks (partials) per reduce: arx.cu `kMaxWorld`, common.cuh `kMaxNumGPU`. */
+#define ARX_MAX_W 8
+/* Most thread blocks per virtual rank in arx_step (bounds the control words). */
+#define ARX_STEP_MAX_BLOCKS 256
+/* Default bound of every device-side wait of arx_step, in nanoseconds. */
+#define ARX_DEFAULT_TIMEOUT_NS 1000000000ull
+
+typedef enum arx_status {
+  ARX_OK = 0,
+  ARX_EINVAL = 1,    /* bad argument: W out of range, null or misaligned pointer, n too large */
+  ARX_EOVERLAP = 2,  /* out partially overlaps an input (only exact aliasing is allowed) */
+  ARX_ECUDA = 3,     /* a CUDA runtime call or kernel launch failed; see arx_last_error() */
+  ARX_ETIMEOUT = 4,  /* a bounded device wait of arx_step expired (reported by arx_ctx_query) */
+  ARX_ESTATE = 5     /* protocol words inconsistent (epoch != completed steps mod 2), or bad ctx */
+} arx_status;
+
+/* One-line name of a status code (static storage). */
+const char* arx_status_string(arx_status s);
+
+/* Detail of the last non-OK status returned to the calling thread, or "". */
+const char* arx_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Stateless reduce.
+ *
+ * out[i] = bf16_rne( (((+0.0f + f32(s0[i])) + f32(s1[i])) + ...) + f32(s{W-1}[i]) )
+ * for 0 <= i < n, every add in fp32 round-to-nearest-even, subnormals kept
+ * (arx.cu, `arx_kernel`, reduce loop).
+ *
+ *   slots   HOST array of W device pointers, each to n bf16 elements.  The
+ *           array itself is read during the call only (it is copied into the
+ *           kernel's parameters).  Slots may repeat or overlap each other.
+ *   W       1 <= W <= ARX_MAX_W.  (The page requires W >= 2; W = 1 is the
+ *           identity, except that -0 becomes +0.)
+ *   out     device pointer to n bf16 elements.  It may be exactly equal to
+ *           one slot pointer ("in and out may alias", arx.cu); any other
+ *           overlap with a slot is ARX_EOVERLAP.
+ *   n       elements per slot.  n == 0 returns ARX_OK and launches nothing
+ *           (pointers are not inspected).  No upper limit besides memory.
+ *   stream  cudaStream_t as void*.
+ * Alignment: every pointer must be 2-byte aligned (ARX_EINVAL otherwise).
+ * When all of them share the same address mod 16 the kernel streams 16-byte
+ * vectors (a scalar head/tail covers the rest); otherwise a scalar kernel runs.
+ * Returns ARX_ECUDA if the launch fails (the stream is left as CUDA left it).
+ * ------------------------------------------------------------------------- */
+arx_status arx_reduce(const void* const* slots, int W, void* out, size_t n, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-buffer form of arx_reduce, for callers whose partials live in host
+ * memory (the end-to-end form: copies in, reduce, copy out, all enqueued on
+ * `stream` in that order).  On arx.cu's GB10 the partials are pinned host
+ * buffers the GPU reads directly; here they are copied into device staging.
+ *
+ *   host_slots     HOST array of W host pointers, each to n bf16 elements.
+ *                  Pinned (cudaHostAlloc / page-locked) memory makes the
+ *                  copies asynchronous; pageable memory works but the
+ *                  copies then synchronise with the host.
+ *   host_out       host pointer to n bf16 elements (written when the stream
+ *                  reaches the final copy; synchronise `stream` before use).
+ *   dev_staging    device buffer of at least arx_reduce_host_staging_bytes(W, n)
+ *                  bytes, 256-byte aligned is best; owned by the caller and
+ *                  overwritten.  Slot r is staged at byte offset r * stride,
+ *                  stride = n*2 rounded up to 256; the sum is written in place
+ *                  over staged slot 0 and copied from there.
+ * One cudaMemcpyAsync per slot, one kernel, one cudaMemcpyAsync back.
+ * Errors as arx_reduce; ARX_EINVAL if the staging buffer is too small.
+ * ------------------------------------------------------------------------- */
+size_t arx_reduce_host_staging_bytes(int W, size_t n);
+arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out, size_t n,
+                           void* dev_staging, size_t staging_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Stateful protocol step: seq/parity double-buffered slots, per-block
+ * Semaphore epochs and a zero-resetting signal pad, run as one kernel.
+ *
+ * The pages synchronise ranks on different GPUs: arx.cu stages each partial
+ * into send[seq & 1] and waits for the peers' flags; common.cuh's
+ * PullController counts per-block Semaphore arrivals (start stage W, end
+ * stage 2W, then counter += 2W) and PushController keeps a per-block parity
+ * epoch; triton_barrier.py's blockwise_barrier leaves its signal pad all zero
+ * after every synchronisation so no host-side flag is needed under CUDA graph
+ * replay.  On one GPU the W ranks are W virtual ranks: the step runs a grid of
+ * B x W thread blocks, block (b, r) playing rank r's block b:
+ *   1. seq = completed + 1, par = seq & 1; check epoch[r][b] == (seq-1) & 1;
+ *   2. start barrier (unfenced): +1 to sem[q][b] for every q, wait for W;
+ *   3. stage input r's chunk b into slots[par][r]; last block publishes seq;
+ *   4. end barrier (release/acquire): +1 to sem[q][b], wait for 2W, counter += 2W;
+ *   5. reduce sub-range r of chunk b over slots[par][0..W-1] into out;
+ *   6. pad barrier (0->1 sends, 1->0 waits), epoch[r][b] ^= 1, last block out
+ *      stores seq as completed.
+ * The output equals arx_reduce's bit for bit.  Every wait is bounded by the
+ * context's timeout; on expiry the block records ARX_ETIMEOUT in the device
+ * error word and carries on, so the kernel always finishes.
+ *
+ * Workspace: one caller-owned device buffer, ZERO-FILLED before the first
+ * step (e.g. torch.zeros(uint8)), of arx_ctx_workspace_bytes(W, max_n,
+ * nblocks) bytes and 256-byte aligned.  Layout (offsets in arx_ctx):
+ *   [0, 256)        header, uint32: seq (completed steps), err (device error
+ *                   word, 0 = none), blocks[2] (publish / exit counters),
+ *                   published (last staged seq)
+ *   off_epoch       uint32 epoch[W][B]                    (PushController)
+ *   off_sem         struct { uint32 flag, counter; } sem[W][B], 128-byte
+ *                   stride                                (Semaphore)
+ *   off_pad         uint32 pad[W][B][W], pad[owner][b][sender]  (signal pad)
+ *   off_slots       bf16 slots[2][W][slot_stride]         (parity x rank)
+ * Device error word: low 8 bits an arx_status, bits 8-11 the stage that
+ * failed (1 start wait, 2 end wait, 3 pad send, 4 pad wait, 5 epoch check),
+ * bits 12-15 the virtual rank, bits 16-31 the block.
+ * ------------------------------------------------------------------------- */
+typedef struct arx_ctx {
+  uint32_t magic;        /* set by arx_ctx_init */
+  int32_t W;             /* virtual ranks, 1..ARX_MAX_W */
+  int32_t nblocks;       /* B, thread blocks per virtual rank */
+  int32_t fault_rank;    /* -1, or a virtual rank that skips its end-barrier signal (testing) */
+  uint64_t max_n;        /* capacity of one slot, elements */
+  uint64_t slot_stride;  /* elements from one slot to the next (multiple of 128) */
+  uint64_t timeout_ns;   /* bound of every device wait */
+  void* ws;              /* device workspace base */
+  uint64_t ws_bytes;
+  uint64_t off_epoch, off_sem, off_pad, off_slots;
+  uint64_t ctrl_bytes;   /* bytes [0, ctrl_bytes) hold every protocol word */
+} arx_ctx;
+
+/* Workspace bytes for W virtual ranks, slots of max_n elements and `nblocks`
+ * blocks per rank (nblocks == 0 sizes for ARX_STEP_MAX_BLOCKS, which fits
+ * any nblocks).  Returns 0 for invalid W or nblocks. */
+size_t arx_ctx_workspace_bytes(int W, size_t max_n, int nblocks);
+
+/* Fills *ctx (a host struct; no allocation, no device access unless
+ * nblocks == 0).  nblocks == 0 picks B from the current device's SM count
+ * and max_n.  The workspace must be zero-filled before the first step, and
+ * after any step that reported an error (see arx_ctx_reset). */
+arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t max_n,
+                        int nblocks);
+
+/* Sets the bound of every device wait (ns > 0). */
+arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
+
+/* Testing knob: virtual rank `rank` (0..W-1) skips its end-barrier signal, so
+ * the step's waits expire and report ARX_ETIMEOUT; -1 turns it off.  No GPU
+ * fault, trap or unbounded wait results. */
+arx_status arx_ctx_set_fault(arx_ctx* ctx, int rank);
+
+/* Enqueues a zero fill of the protocol words [0, ctrl_bytes) (not the slots):
+ * seq, epochs, Semaphores, pad and the error word all return to zero. */
+arx_status arx_ctx_reset(const arx_ctx* ctx, void* stream);
+
+/* One protocol step: out = rank-order reduce of inputs[0..W-1].
+ *   inputs  HOST array of ctx->W device pointers, each to n bf16 elements.
+ *   out     device pointer to n bf16; may equal one input exactly; must not
+ *           overlap the workspace.
+ *   n       0 < n <= ctx->max_n (n == 0 returns ARX_OK, no launch).
+ * Steps on one context must be serialised (one stream, or events). */
+arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, size_t n,
+                    void* stream);
+
+/* Synchronises `stream`, then reads the header: *seq = completed steps,
+ * *dev_err = device error word (either pointer may be NULL).  Returns the
+ * status in the error word's low 8 bits (ARX_OK when it is 0), or ARX_ECUDA. */
+arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ARX_H_ */

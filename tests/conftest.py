@@ -23,6 +23,14 @@ def gpu_available() -> bool:
 
 @pytest.fixture(scope="session")
 def product_lib_path():
-    """Builds (if stale) and returns the path of the C-ABI library."""
-    from deterministic_shot_all_gb300 import _build
-    return _build.build()
+    """Builds (if stale) the C-ABI library and the oracle; returns the library path."""
+    import __graft_entry__
+    __graft_entry__.build()
+    return os.path.join(ROOT, "deterministic_shot_all_gb300", "libarx.so")
+
+
+@pytest.fixture(scope="session")
+def arx(product_lib_path):
+    """The Python binding of the C ABI (loads libarx.so)."""
+    import deterministic_shot_all_gb300
+    return deterministic_shot_all_gb300

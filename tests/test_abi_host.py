@@ -1,0 +1,154 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+* the library loads and exports every function ``include/arx.h`` declares;
+* argument validation returns the documented status before touching CUDA;
+* the protocol context's workspace layout is consistent.
+
+Addresses used here are fabricated integers: every call below is rejected (or
+needs no device) before anything could dereference them.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT, gpu_available
+
+HEADER = os.path.join(ROOT, "include", "arx.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(arx_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for must in ("arx_reduce", "arx_step", "arx_ctx_init", "arx_ctx_query",
+                 "arx_ctx_workspace_bytes", "arx_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(product_lib_path):
+    lib = ctypes.CDLL(product_lib_path)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in arx.h but not exported: {missing}"
+
+
+def test_status_strings(arx):
+    for code in range(6):
+        assert arx.arx_status_string(code).startswith("ARX_")
+    assert "unknown" in arx.arx_status_string(99)
+
+
+FAKE = 1 << 40  # 16-byte aligned fabricated address
+
+
+def _reduce(arx, slots, W, out, n):
+    arr = (ctypes.c_void_p * max(1, len(slots)))(*slots) if slots else None
+    return arx.lib.arx_reduce(arr, W, out, n, None)
+
+
+def test_reduce_n0_is_a_no_op_even_with_null_pointers(arx):
+    assert arx.lib.arx_reduce(None, 0, None, 0, None) == arx.ARX_OK
+
+
+@pytest.mark.parametrize("W", [0, -1, 9, 100])
+def test_reduce_rejects_w_out_of_range(arx, W):
+    slots = [FAKE + 4096 * i for i in range(max(W, 1))][:8]
+    assert _reduce(arx, slots, W, FAKE + (1 << 30), 16) == arx.ARX_EINVAL
+
+
+def test_reduce_rejects_null_and_misaligned_pointers(arx):
+    out = FAKE + (1 << 30)
+    assert _reduce(arx, [FAKE, 0], 2, out, 16) == arx.ARX_EINVAL
+    assert _reduce(arx, [FAKE, FAKE + 4096], 2, 0, 16) == arx.ARX_EINVAL
+    assert _reduce(arx, [FAKE + 1, FAKE + 4096], 2, out, 16) == arx.ARX_EINVAL
+    assert _reduce(arx, [FAKE, FAKE + 4096], 2, out + 1, 16) == arx.ARX_EINVAL
+    assert "aligned" in arx.arx_last_error()
+
+
+def test_reduce_rejects_partial_overlap(arx):
+    n = 1024
+    a, b = FAKE, FAKE + 4 * n
+    assert _reduce(arx, [a, b], 2, a + 2, n) == arx.ARX_EOVERLAP   # shifted by one element
+    assert _reduce(arx, [a, b], 2, b - 2 * n + 2, n) == arx.ARX_EOVERLAP
+    assert "overlap" in arx.arx_last_error()
+
+
+@pytest.mark.skipif(gpu_available(), reason="checks the no-device error path")
+def test_reduce_without_a_device_reports_cuda_error(arx):
+    n = 1024
+    st = _reduce(arx, [FAKE, FAKE + 4 * n], 2, FAKE, n)  # exact alias: valid arguments
+    assert st == arx.ARX_ECUDA
+    assert arx.arx_last_error()
+
+
+def test_staging_bytes(arx):
+    assert arx.arx_reduce_host_staging_bytes(8, 131072) == 8 * 262144
+    assert arx.arx_reduce_host_staging_bytes(3, 5) == 3 * 256
+    assert arx.arx_reduce_host_staging_bytes(0, 5) == 0
+    assert arx.arx_reduce_host_staging_bytes(9, 5) == 0
+
+
+def test_workspace_layout(arx):
+    W, n, B = 8, 131072, 19
+    nbytes = arx.arx_ctx_workspace_bytes(W, n, B)
+    assert nbytes > 2 * W * n * 2
+    assert arx.arx_ctx_workspace_bytes(W, n, 0) >= nbytes  # sized for the block maximum
+    assert arx.arx_ctx_workspace_bytes(0, n, B) == 0
+    assert arx.arx_ctx_workspace_bytes(W, n, arx.ARX_STEP_MAX_BLOCKS + 1) == 0
+    ctx = arx.arx_ctx()
+    st = arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, nbytes, W, n, B)
+    assert st == arx.ARX_OK
+    assert ctx.W == W and ctx.nblocks == B and ctx.fault_rank == -1
+    assert ctx.timeout_ns == arx.ARX_DEFAULT_TIMEOUT_NS
+    assert ctx.off_epoch >= 20                                 # after the header words
+    assert ctx.off_sem >= ctx.off_epoch + W * B * 4 and ctx.off_sem % 128 == 0
+    assert ctx.off_pad >= ctx.off_sem + W * B * 128
+    assert ctx.off_slots >= ctx.off_pad + W * B * W * 4 and ctx.off_slots % 256 == 0
+    assert ctx.slot_stride >= n and ctx.slot_stride % 128 == 0
+    assert ctx.ctrl_bytes == ctx.off_slots
+    assert ctx.off_slots + 2 * W * ctx.slot_stride * 2 == nbytes
+
+
+def test_ctx_init_rejections(arx):
+    ctx = arx.arx_ctx()
+    nbytes = arx.arx_ctx_workspace_bytes(4, 1000, 4)
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE + 16, nbytes, 4, 1000, 4) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, nbytes - 1, 4, 1000, 4) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), 0, nbytes, 4, 1000, 4) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, nbytes, 9, 1000, 4) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, nbytes, 4, 1000, -1) == arx.ARX_EINVAL
+
+
+def test_ctx_knobs_and_step_validation(arx):
+    W, n, B = 4, 4096, 2
+    nbytes = arx.arx_ctx_workspace_bytes(W, n, B)
+    ctx = arx.arx_ctx()
+    # An uninitialised context is refused.
+    assert arx.lib.arx_step(ctypes.byref(ctx), None, FAKE, 16, None) == arx.ARX_ESTATE
+    assert arx.lib.arx_ctx_set_timeout(ctypes.byref(ctx), 5) == arx.ARX_ESTATE
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, nbytes, W, n, B) == arx.ARX_OK
+    assert arx.lib.arx_ctx_set_timeout(ctypes.byref(ctx), 0) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_set_timeout(ctypes.byref(ctx), 12345) == arx.ARX_OK
+    assert ctx.timeout_ns == 12345
+    assert arx.lib.arx_ctx_set_fault(ctypes.byref(ctx), W) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_set_fault(ctypes.byref(ctx), -2) == arx.ARX_EINVAL
+    assert arx.lib.arx_ctx_set_fault(ctypes.byref(ctx), 1) == arx.ARX_OK and ctx.fault_rank == 1
+    assert arx.lib.arx_ctx_set_fault(ctypes.byref(ctx), -1) == arx.ARX_OK
+    ins = (ctypes.c_void_p * W)(*[FAKE + (1 << 32) + i * (1 << 20) for i in range(W)])
+    # n == 0: nothing to do.
+    assert arx.lib.arx_step(ctypes.byref(ctx), ins, FAKE + (1 << 34), 0, None) == arx.ARX_OK
+    # n beyond the slot capacity.
+    assert arx.lib.arx_step(ctypes.byref(ctx), ins, FAKE + (1 << 34), n + 1, None) == arx.ARX_EINVAL
+    # Output inside the workspace.
+    assert arx.lib.arx_step(ctypes.byref(ctx), ins, FAKE + 256, n, None) == arx.ARX_EOVERLAP
+    # Output partially overlapping an input.
+    assert arx.lib.arx_step(ctypes.byref(ctx), ins, ins[1] + 2, n, None) == arx.ARX_EOVERLAP
+    # Null input.
+    bad = (ctypes.c_void_p * W)(*([0] + list(ins[1:])))
+    assert arx.lib.arx_step(ctypes.byref(ctx), bad, FAKE + (1 << 34), n, None) == arx.ARX_EINVAL

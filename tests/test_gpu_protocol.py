@@ -1,0 +1,277 @@
+"""GPU tests of the protocol step (``arx_step``) against the oracle and its model.
+
+* Output: bit-exact against the oracle's rank-order reduce (and therefore
+  against ``arx_reduce``) for every W, ragged n and misaligned buffers.
+* Protocol words after k steps equal the oracle's sequential model
+  (oracle/protocol.py): seq, per-block epochs, Semaphore flag == counter
+  (common.cuh, ``PullController::sync``), the signal pad all zero
+  (triton_barrier.py, ``barrier_test``'s assertion), both block counters
+  back at zero (arx.cu), and the two slot banks holding the last two steps'
+  inputs (arx.cu: two buffers by parity).
+* Unsigned wrap of seq and flags.
+* 10,000 steps captured in one CUDA graph with fresh partials per step.
+* Failure detection without any GPU fault: a missing end-barrier signal
+  makes the bounded waits expire (ARX_ETIMEOUT read by the host, context
+  usable after a reset); a corrupted epoch reports ARX_ESTATE.
+"""
+
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import protocol as model
+import synthetic_partials as sp
+from test_gpu_reduce import assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+
+M32 = 0xFFFFFFFF
+
+
+@pytest.fixture(scope="module")
+def dev(arx):
+    assert torch.cuda.is_available(), "these tests need a GPU"
+    return torch.device("cuda:0")
+
+
+class Ctx:
+    """A context plus typed views of its workspace words."""
+
+    def __init__(self, arx, dev, W, max_n, nblocks=0):
+        self.arx = arx
+        nbytes = arx.arx_ctx_workspace_bytes(W, max_n, nblocks)
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        self.ctx = arx.arx_ctx_init(self.ws, W, max_n, nblocks)
+        self.W, self.B = W, self.ctx.nblocks
+
+    def words(self):
+        c, W, B = self.ctx, self.W, self.B
+        host = self.ws[: c.ctrl_bytes].cpu().numpy()
+        u32 = lambda off, cnt: host[off: off + 4 * cnt].view(np.uint32).astype(np.int64)
+        hdr = u32(0, 5)
+        sem = host[c.off_sem: c.off_sem + 128 * W * B].reshape(W * B, 128)[:, :8].copy().view(np.uint32)
+        return dict(seq=int(hdr[0]), err=int(hdr[1]), blocks=[int(hdr[2]), int(hdr[3])],
+                    published=int(hdr[4]), epoch=u32(c.off_epoch, W * B).reshape(W, B),
+                    flag=sem[:, 0].astype(np.int64).reshape(W, B),
+                    counter=sem[:, 1].astype(np.int64).reshape(W, B),
+                    pad=u32(c.off_pad, W * B * W).reshape(W, B, W))
+
+    def slot(self, par, r, n):
+        c = self.ctx
+        off = c.off_slots + (par * self.W + r) * c.slot_stride * 2
+        return self.ws[off: off + 2 * n].cpu().numpy().view(np.uint16)
+
+    def poke(self, off, value):
+        self.ws[off: off + 4] = torch.tensor([value], dtype=torch.int64).view(torch.uint8)[:4].to(self.ws.device)
+
+
+def _compare_to_model(words, st: model.State):
+    assert words["seq"] == st.seq and words["published"] == st.published
+    assert words["blocks"] == st.blocks
+    assert (words["err"] & 0xFF) == st.err
+    assert np.array_equal(words["epoch"], st.epoch)
+    assert np.array_equal(words["flag"], st.flag)
+    assert np.array_equal(words["counter"], st.counter)
+    assert np.array_equal(words["pad"], st.pad)
+
+
+def _step(arx, c: Ctx, x: torch.Tensor, dev, out_offset=0, in_offset=0):
+    W, n = x.shape
+    if in_offset:
+        buf = torch.zeros(W, n + 8, dtype=torch.bfloat16, device=dev)
+        buf[:, in_offset:in_offset + n] = x.to(dev)
+        ins = [buf[r, in_offset:in_offset + n] for r in range(W)]
+    else:
+        xd = x.to(dev)
+        ins = [xd[r] for r in range(W)]
+    ob = torch.zeros(n + 16, dtype=torch.bfloat16, device=dev)
+    out = ob[out_offset:out_offset + n]
+    arx.arx_step(c.ctx, ins, out)
+    return out
+
+
+@pytest.mark.parametrize("W", range(1, 9))
+def test_single_step_every_w(arx, dev, W):
+    for n, nblocks in ((131072, 0), (1000003, 0), (13, 1), (4096 + 5, 3)):
+        c = Ctx(arx, dev, W, n, nblocks)
+        x = sp.partials(W, n, "special" if n < 5000 else "normal", seed=W * 7 + n)
+        out = _step(arx, c, x, dev)
+        st, seq, err = arx.arx_ctx_query(c.ctx)
+        assert (st, seq, err) == (arx.ARX_OK, 1, 0)
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                          f"step W={W} n={n} B={c.B}")
+
+
+def test_step_equals_stateless_reduce(arx, dev):
+    x, _ = sp.workload("w8_32x4096_normal")
+    xd = x.to(dev)
+    c = Ctx(arx, dev, 8, x.shape[1])
+    a = torch.empty(x.shape[1], dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    arx.arx_reduce([xd[r] for r in range(8)], a)
+    arx.arx_step(c.ctx, [xd[r] for r in range(8)], b)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("in_off,out_off", [(1, 0), (0, 3), (5, 5)])
+def test_step_misaligned_buffers(arx, dev, in_off, out_off):
+    W, n = 4, 20011
+    c = Ctx(arx, dev, W, n)
+    x = sp.partials(W, n, "normal", seed=in_off * 10 + out_off)
+    out = _step(arx, c, x, dev, out_offset=out_off, in_offset=in_off)
+    assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                      f"offsets in={in_off} out={out_off}")
+
+
+def test_step_output_aliases_an_input(arx, dev):
+    W, n = 3, 50000
+    c = Ctx(arx, dev, W, n)
+    x = sp.partials(W, n, "normal", seed=31)
+    xd = x.to(dev)
+    ins = [xd[r] for r in range(W)]
+    arx.arx_step(c.ctx, ins, ins[1])
+    assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+    assert_bits_equal(xd[1].cpu().view(torch.int16).numpy(),
+                      oracle.reduce(list(sp.to_u16_numpy(x))), "step in place")
+
+
+@pytest.mark.parametrize("W,n,B,k", [(8, 131072, 0, 5), (3, 777, 2, 4), (5, 65536 + 7, 7, 3), (1, 100, 1, 2)])
+def test_protocol_words_follow_the_model(arx, dev, W, n, B, k):
+    c = Ctx(arx, dev, W, n, B)
+    st = model.State(W=W, B=c.B)
+    hist = []
+    for s in range(k):
+        x = sp.partials(W, n, "normal", seed=4 + s)
+        u = list(sp.to_u16_numpy(x))
+        hist.append(u)
+        out = _step(arx, c, x, dev)
+        want = model.step(st, u)
+        assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s}")
+        _compare_to_model(c.words(), st)
+    assert (c.words()["flag"] == 2 * W * k).all()
+    for r in range(W):
+        assert np.array_equal(c.slot(k & 1, r, n), hist[k - 1][r])
+        if k >= 2:
+            assert np.array_equal(c.slot((k - 1) & 1, r, n), hist[k - 2][r])
+
+
+def test_unsigned_wrap_of_seq_and_flags(arx, dev):
+    W, n, B = 8, 4096, 4
+    c = Ctx(arx, dev, W, n, B)
+    seq0, flag0 = M32 - 1, M32 - 5
+    c.poke(0, seq0)
+    ctx = c.ctx
+    for i in range(W * B):
+        c.poke(ctx.off_sem + 128 * i, flag0)
+        c.poke(ctx.off_sem + 128 * i + 4, flag0)
+        c.poke(ctx.off_epoch + 4 * i, seq0 % 2)
+    st = model.State(W=W, B=B, seq=seq0)
+    st.epoch[:] = seq0 % 2
+    st.flag[:] = flag0
+    st.counter[:] = flag0
+    st.published = 0
+    for s in range(3):
+        x = sp.partials(W, n, "normal", seed=50 + s)
+        out = _step(arx, c, x, dev)
+        want = model.step(st, list(sp.to_u16_numpy(x)))
+        assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"wrap step {s}")
+    w = c.words()
+    _compare_to_model(w, st)
+    assert w["seq"] == 1
+
+
+def test_timeout_is_reported_and_context_recovers(arx, dev):
+    W, n = 4, 8192
+    c = Ctx(arx, dev, W, n, 2)
+    x = sp.partials(W, n, "normal", seed=8)
+    _step(arx, c, x, dev)
+    assert arx.arx_ctx_query(c.ctx)[:2] == (arx.ARX_OK, 1)
+    arx.arx_ctx_set_timeout(c.ctx, 20_000_000)      # 20 ms bound on every wait
+    arx.arx_ctx_set_fault(c.ctx, 2)                 # virtual rank 2 never sends its end signal
+    _step(arx, c, x, dev)
+    st, seq, err = arx.arx_ctx_query(c.ctx)
+    assert st == arx.ARX_ETIMEOUT
+    assert err & 0xFF == arx.ARX_ETIMEOUT and (err >> 8) & 15 == 2  # stage: end-barrier wait
+    assert seq == 2                                  # the kernel still finished
+    w = c.words()
+    assert not w["pad"].any() and w["blocks"] == [0, 0]
+    # Recovery: zero the protocol words, clear the fault, step again.
+    arx.arx_ctx_set_fault(c.ctx, -1)
+    arx.arx_ctx_reset(c.ctx)
+    out = _step(arx, c, x, dev)
+    assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, 1, 0)
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                      "after reset")
+
+
+def test_epoch_mismatch_reports_state_error(arx, dev):
+    W, n = 2, 1024
+    c = Ctx(arx, dev, W, n, 2)
+    c.poke(c.ctx.off_epoch + 4 * 3, 1)   # epoch[1][1] claims an odd step count
+    x = sp.partials(W, n, "normal", seed=2)
+    out = _step(arx, c, x, dev)
+    st, seq, err = arx.arx_ctx_query(c.ctx)
+    assert st == arx.ARX_ESTATE and (err >> 8) & 15 == 5 and (err >> 12) & 15 == 1
+    # The data path is unaffected.
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))), "data")
+
+
+# ---- 10,000 steps in one CUDA graph --------------------------------------------------------
+
+GRAPH_STEPS = sp.GRAPH_STEPS
+W8, N8 = 8, sp.N_32x4096
+
+
+def test_ten_thousand_steps_in_one_graph(arx, dev):
+    steps, chunk = GRAPH_STEPS, 500
+    c = Ctx(arx, dev, W8, N8)
+    inputs = torch.empty(steps, W8, N8, dtype=torch.bfloat16, device=dev)
+    outputs = torch.zeros(steps, N8, dtype=torch.bfloat16, device=dev)
+    want = np.empty((steps, N8), dtype=np.uint16)
+    last_two = {}
+    host = torch.empty(chunk, W8, N8, dtype=torch.int16).pin_memory()
+    host_np = host.numpy().view(np.uint16)
+
+    # Step s draws fresh normal(0, 1) partials from seed 4 + s.  Torch's RNG and
+    # the oracle's C code release the GIL, so threads generate in parallel.
+    def fill(s, base):
+        u = sp.to_u16_numpy(sp.graph_step_partials(s))
+        host_np[s - base] = u
+        want[s] = oracle.reduce_rows(u)
+        if s >= steps - 2:
+            last_two[s] = u.copy()
+
+    with ThreadPoolExecutor(max_workers=min(16, oracle.default_threads())) as ex:
+        for base in range(0, steps, chunk):
+            hi = min(steps, base + chunk)
+            list(ex.map(lambda s: fill(s, base), range(base, hi)))
+            inputs[base:hi].view(torch.int16).copy_(host[: hi - base])
+    torch.cuda.synchronize()
+
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(steps):
+            arx.arx_step(c.ctx, [inputs[t, r] for r in range(W8)], outputs[t], stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    st, seq, err = arx.arx_ctx_query(c.ctx)
+    assert (st, seq, err) == (arx.ARX_OK, steps, 0)
+    got = outputs.cpu().view(torch.int16).numpy().view(np.uint16)
+    bad = np.flatnonzero((got != want).any(axis=1))
+    assert bad.size == 0, f"{bad.size} of {steps} steps differ; first step {int(bad[0])}"
+    w = c.words()
+    assert not w["pad"].any(), "signal pad must be all zero after the last step"
+    assert (w["flag"] == 2 * W8 * steps).all() and (w["counter"] == w["flag"]).all()
+    assert (w["epoch"] == steps % 2).all() and w["blocks"] == [0, 0]
+    assert w["published"] == steps
+    for r in range(W8):
+        assert np.array_equal(c.slot(steps & 1, r, N8), last_two[steps - 1][r])
+        assert np.array_equal(c.slot((steps - 1) & 1, r, N8), last_two[steps - 2][r])

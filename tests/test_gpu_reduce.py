@@ -1,0 +1,229 @@
+"""GPU parity of the stateless reduce (``arx_reduce``) against the CPU oracle.
+
+Bar: bit-exact (integer comparison of the bf16 patterns) on every element;
+NaN outputs compare by NaN-ness only (the payload is unpinned, as the oracle
+header states).  Every call goes through the C ABI via the binding.
+
+Covers the workloads the one-shot all-reduce targets -- W = 2, 4, 8 partials
+of bf16 [32, 4096] and [1024, 8192] (arx.cu, ``kMaxBytes`` comment, widened),
+the in-place form (arx.cu: "in and out may alias"), the power-of-two size
+sweep from 1 KiB to 256 MiB per partial -- plus ragged sizes, every W,
+misaligned pointers, hard floating-point patterns and guard bytes.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_partials as sp
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 64
+SENTINEL = 0x7E57
+
+
+def _is_nan16(b):
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+
+
+def assert_bits_equal(got: np.ndarray, want: np.ndarray, what: str = ""):
+    got = got.view(np.uint16)
+    want = want.view(np.uint16)
+    assert got.shape == want.shape
+    nan_w = _is_nan16(want)
+    same = (got == want) | (nan_w & _is_nan16(got))
+    if not same.all():
+        bad = np.flatnonzero(~same)
+        i = int(bad[0])
+        pytest.fail(f"{what}: {bad.size} of {got.size} elements differ; first at {i}: "
+                    f"gpu {int(got[i]):#06x} oracle {int(want[i]):#06x}")
+
+
+@pytest.fixture(scope="module")
+def dev(arx):
+    assert torch.cuda.is_available(), "these tests need a GPU"
+    return torch.device("cuda:0")
+
+
+def _run(arx, dev, x: torch.Tensor, alias: bool = False) -> np.ndarray:
+    """Reduce the [W, n] CPU bf16 partials on the GPU; returns the output patterns."""
+    W, n = x.shape
+    xd = x.to(dev)
+    slots = [xd[r] for r in range(W)]
+    if alias:
+        out = slots[0]
+    else:
+        buf = torch.full((n + 2 * GUARD,), 0, dtype=torch.int16, device=dev)
+        buf.fill_(SENTINEL)
+        out = buf[GUARD:GUARD + n].view(torch.bfloat16)
+    arx.arx_reduce(slots, out)
+    torch.cuda.synchronize()
+    if not alias:
+        g = buf.cpu().numpy().view(np.uint16)
+        assert (g[:GUARD] == SENTINEL).all() and (g[GUARD + n:] == SENTINEL).all(), "guard bytes written"
+    for r in range(1 if alias else 0, W):  # inputs other than the aliased slot are untouched
+        assert torch.equal(xd[r].cpu().view(torch.int16), x[r].view(torch.int16))
+    return out.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("name", ["w2_32x4096_uniform", "w8_32x4096_normal"])
+def test_decode_sized_workloads(arx, dev, name):
+    x, alias = sp.workload(name)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    assert_bits_equal(_run(arx, dev, x, alias), want, name)
+
+
+def test_in_place_1024x8192_w4(arx, dev):
+    x, alias = sp.workload("w4_1024x8192_alias")
+    assert alias
+    want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+    got = _run(arx, dev, x, alias=True)   # first call on a pristine copy
+    assert_bits_equal(got, want, "w4 [1024,8192] in place")
+
+
+@pytest.mark.parametrize("k", list(sp.SWEEP_LOG2))
+def test_size_sweep_integer_partials(arx, dev, k):
+    n = 1 << k
+    x, _ = sp.workload("w8_sweep_int", n=n)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+    got = _run(arx, dev, x)
+    assert_bits_equal(got, want, f"sweep n=2^{k}")
+    # Integer partials in [-8, 8]: the sum is exact, check it against integers too.
+    if k <= 20:
+        exact = x.to(torch.int64).sum(0).to(torch.float32).to(torch.bfloat16)
+        assert_bits_equal(got, sp.to_u16_numpy(exact), "exact integer sum")
+
+
+@pytest.mark.parametrize("W", range(1, 9))
+def test_every_w_with_hard_patterns(arx, dev, W):
+    # Random bit patterns: subnormals, infinities, NaN, signed zeros, ties.
+    for n in (1, 7, 8, 9, 255, 4099, 70001):
+        x = sp.partials(W, n, "special", seed=1000 * W + n)
+        want = oracle.reduce(list(sp.to_u16_numpy(x)))
+        assert_bits_equal(_run(arx, dev, x), want, f"W={W} n={n}")
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+def test_in_place_small_and_ragged(arx, dev, W):
+    for n in (1, 5, 8, 13, 1000, 65537):
+        x = sp.partials(W, n, "normal", seed=77 + n)
+        want = oracle.reduce(list(sp.to_u16_numpy(x)))
+        assert_bits_equal(_run(arx, dev, x, alias=True), want, f"alias W={W} n={n}")
+
+
+def test_alias_to_last_slot(arx, dev):
+    x = sp.partials(5, 40000, "normal", seed=9)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    xd = x.to(dev)
+    slots = [xd[r] for r in range(5)]
+    arx.arx_reduce(slots, slots[4])
+    torch.cuda.synchronize()
+    assert_bits_equal(xd[4].cpu().view(torch.int16).numpy(), want, "alias slot 4")
+
+
+@pytest.mark.parametrize("offsets", [
+    (1, 1, 1),          # same misalignment: vector path with a scalar head
+    (3, 3, 3),
+    (7, 7, 7),
+    (0, 1, 0),          # mixed: scalar path
+    (2, 5, 1),
+    (0, 0, 4),          # output misaligned only
+])
+def test_misaligned_pointers(arx, dev, offsets):
+    W, n = 2, 10007
+    x = sp.partials(W, n, "uniform", seed=sum(offsets))
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    bufs = []
+    slots = []
+    for r in range(W):
+        b = torch.zeros(n + 16, dtype=torch.bfloat16, device=dev)
+        b[offsets[r]:offsets[r] + n] = x[r].to(dev)
+        bufs.append(b)
+        slots.append(b[offsets[r]:offsets[r] + n])
+    ob = torch.full((n + 16 + 2 * GUARD,), SENTINEL, dtype=torch.int16, device=dev)
+    o0 = GUARD + offsets[2]
+    out = ob[o0:o0 + n].view(torch.bfloat16)
+    arx.arx_reduce(slots, out)
+    torch.cuda.synchronize()
+    g = ob.cpu().numpy().view(np.uint16)
+    assert (g[:o0] == SENTINEL).all() and (g[o0 + n:] == SENTINEL).all()
+    assert_bits_equal(g[o0:o0 + n], want, f"offsets {offsets}")
+
+
+def test_w1_identity_and_negative_zero(arx, dev):
+    x = sp.partials(1, 100003, "special", seed=4)
+    got = _run(arx, dev, x)
+    u = sp.to_u16_numpy(x)[0]
+    nan = _is_nan16(u)
+    want = np.where(u == 0x8000, np.uint16(0), u)
+    assert np.array_equal(_is_nan16(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    nz = torch.full((3, 4096), -0.0, dtype=torch.bfloat16)
+    assert not _run(arx, dev, nz).any(), "(-0) + (-0) + (-0) from +0 must be +0"
+
+
+def test_subnormals_are_not_flushed(arx, dev):
+    tiny = torch.from_numpy(np.array([0x0001, 0x0003, 0x007F, 0x8001], dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    x = torch.stack([tiny, tiny])
+    got = _run(arx, dev, x)
+    assert list(got) == [0x0002, 0x0006, 0x00FE, 0x8002]
+
+
+def test_repeated_slot_pointer(arx, dev):
+    x = sp.partials(1, 5000, "normal", seed=3)
+    xd = x.to(dev)
+    out = torch.empty(5000, dtype=torch.bfloat16, device=dev)
+    arx.arx_reduce([xd[0]] * 3, out)
+    torch.cuda.synchronize()
+    u = sp.to_u16_numpy(x)[0]
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce([u, u, u]), "slot repeated")
+
+
+def test_partial_overlap_is_rejected_on_device_buffers(arx, dev):
+    x = torch.zeros(2, 1024, dtype=torch.bfloat16, device=dev)
+    st = arx.arx_reduce([x[0], x[1]], x.view(-1)[1:1025], check=False)
+    assert st == arx.ARX_EOVERLAP
+
+
+def test_zero_length_launches_nothing(arx, dev):
+    x = torch.zeros(2, 0, dtype=torch.bfloat16, device=dev)
+    assert arx.arx_reduce([x[0], x[1]], x[0], n=0, check=False) == arx.ARX_OK
+
+
+def test_nondefault_stream_and_graph_capture(arx, dev):
+    x, _ = sp.workload("w8_32x4096_normal")
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    xd = x.to(dev)
+    slots = [xd[r] for r in range(8)]
+    outs = torch.zeros(16, x.shape[1], dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        arx.arx_reduce(slots, outs[0], stream=s)       # warm the launch caches off-capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(16):
+            arx.arx_reduce(slots, outs[i], stream=s)
+    outs.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(16):
+        assert_bits_equal(outs[i].cpu().view(torch.int16).numpy(), want, f"graph call {i}")
+
+
+def test_host_buffer_form(arx, dev):
+    W, n = 8, 131072 + 3
+    x = sp.partials(W, n, "normal", seed=21)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    host = [x[r].clone().pin_memory() for r in range(W)]
+    hout = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    staging = torch.empty(arx.arx_reduce_host_staging_bytes(W, n), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        hout.zero_()
+        arx.arx_reduce_host(host, hout, staging)
+        torch.cuda.current_stream().synchronize()
+        assert_bits_equal(hout.view(torch.int16).numpy(), want, "host form")
+    small = torch.empty(arx.arx_reduce_host_staging_bytes(W, n) - 2, dtype=torch.uint8, device=dev)
+    assert arx.arx_reduce_host(host, hout, small, check=False) == arx.ARX_EINVAL
