@@ -277,23 +277,26 @@ def timed_graph_calls(torch, stream, fn, steps: int, warmup: int, chunk: int = G
     g_full = _graph_of_calls(torch, stream, fn, chunk)
     rem = steps % chunk
     g_rem = _graph_of_calls(torch, stream, lambda i: fn(steps - rem + i), rem) if rem else None
-    # Warm-up replays (untimed): at least `warmup` calls.
-    for _ in range(max(1, (warmup + chunk - 1) // chunk)):
-        g_full.replay()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.mark_start()
-    start.record(stream)
-    for _ in range(steps // chunk):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    end.record(stream)
-    torch.cuda.synchronize()
+    # CUDAGraph.replay() launches on torch's current stream: make it `stream`,
+    # the stream the events are recorded on.
+    with torch.cuda.stream(stream):
+        # Warm-up replays (untimed): at least `warmup` calls.
+        for _ in range(max(1, (warmup + chunk - 1) // chunk)):
+            g_full.replay()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_start()
+        start.record(stream)
+        for _ in range(steps // chunk):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
     if sampler:
         sampler.mark_end()
     barrier()
@@ -470,6 +473,47 @@ def e2e_point(torch, arx, sp, dev, stream, workload, steps) -> dict:
             "path": "arx_reduce_host: W cudaMemcpyAsync from pinned host, reduce, 1 copy back"}
 
 
+def run_sweep(args) -> None:
+    """GB/s vs per-partial size for the integer sweep workload (W = 8, n = 2^9 .. 2^27).
+
+    Same timing method as the headline (graph replays, rotation footprint
+    above 3x L2).  Values are drawn on the device (timing only; parity at every
+    size is in the tests).  Prints one JSON object.
+    """
+    import torch
+    import deterministic_shot_all_gb300 as arx
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    stream = torch.cuda.Stream(device=dev)
+    peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+    W = args.sweep_w
+    pts = []
+    for k in range(args.sweep_min, args.sweep_max + 1):
+        n = 1 << k
+        set_bytes = (W + 1) * n * 2
+        R = rotation_sets(set_bytes, l2)
+        gen = torch.Generator(device=dev).manual_seed(3)
+        parts = torch.randint(-8, 9, (R, W, n), generator=gen, device=dev).to(torch.bfloat16)
+        outs = torch.empty(R, n, dtype=torch.bfloat16, device=dev)
+        lists = [[parts[j, r] for r in range(W)] for j in range(R)]
+
+        def call(i, lists=lists, outs=outs, R=R):
+            arx.arx_reduce(lists[i % R], outs[i % R], stream=stream)
+
+        calls = int(min(20000, max(20, 2e9 // set_bytes)))
+        t = timed_graph_calls(torch, stream, call, calls, 20, chunk=min(calls, GRAPH_CALLS))
+        g = gbs(set_bytes, t / calls)
+        pts.append({"log2_n": k, "n": n, "partial_bytes": 2 * n, "calls": calls,
+                    "us_per_call": t / calls * 1e6, "GBs": g, "frac": g / peak})
+        del parts, outs, lists
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "arx_reduce", "W": W, "peak_GBs": peak,
+                      "peak_source": "of measured" if measured_peaks().get("hbm_gbs") else "of fallback",
+                      "points": pts}), flush=True)
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -483,12 +527,18 @@ def main(argv=None) -> None:
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-check", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--sweep", action="store_true", help="GB/s vs size curve instead of the headline")
+    p.add_argument("--sweep-w", type=int, default=8)
+    p.add_argument("--sweep-min", type=int, default=9)
+    p.add_argument("--sweep-max", type=int, default=27)
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
     if args.steps < 1:
         p.error("--steps must be >= 1")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)
