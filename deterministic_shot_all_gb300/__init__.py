@@ -31,6 +31,7 @@ ARX_OK, ARX_EINVAL, ARX_EOVERLAP, ARX_ECUDA, ARX_ETIMEOUT, ARX_ESTATE = range(6)
 ARX_MAX_W = 8
 ARX_STEP_MAX_BLOCKS = 256
 ARX_DEFAULT_TIMEOUT_NS = 1_000_000_000
+ARX_NOALLOC_MAX_N = 131072
 
 
 class ArxError(RuntimeError):
@@ -81,6 +82,7 @@ def _load() -> ctypes.CDLL:
         "arx_ctx_reset": ([ctxp, vp], i32),
         "arx_step": ([ctxp, ptrs, vp, sz, vp], i32),
         "arx_ctx_query": ([ctxp, u32p, u32p, vp], i32),
+        "arx_step_noalloc": ([ptrs, i32, vp, sz, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -208,8 +210,23 @@ def arx_ctx_query(ctx: arx_ctx, stream=None) -> tuple[int, int, int]:
     return st, seq.value, err.value
 
 
+def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=None, stream=None,
+                     check: bool = True) -> int:
+    """Enqueue one protocol step whose workspace is the library's static array (no allocation).
+
+    ``dev_status``: optional device int32/uint32 tensor (or address) that
+    receives the step's device error word.  n is limited to ARX_NOALLOC_MAX_N.
+    """
+    st = lib.arx_step_noalloc(_ptr_array(inputs), len(inputs), _ptr(out), _numel(n, out),
+                              _ptr(dev_status) if dev_status is not None else None, _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
 __all__ = [
     "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce",
     "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
     "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_reset", "arx_step", "arx_ctx_query",
+    "arx_step_noalloc",
 ]

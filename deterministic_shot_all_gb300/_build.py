@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libarx.so")
 
-SOURCES = ["reduce.cu", "step.cu", "abi.cu"]
+SOURCES = ["reduce.cu", "step.cu", "abi.cu", "step_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("arx_device.cuh", "arx_internal.h")] + [
     os.path.join(INCLUDE, "arx.h")]
 

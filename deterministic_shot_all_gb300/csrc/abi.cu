@@ -68,6 +68,24 @@ arx_status check_io(const void* const* in, int W, const void* out, size_t n, boo
 
 }  // namespace
 
+namespace arx {
+
+// For entry points defined in other translation units: the same argument
+// checks and per-thread error text as the entry points here.
+arx_status validate_io(const void* const* in, int W, const void* out, size_t n, bool* out_alias) {
+  return check_io(in, W, out, n, out_alias);
+}
+
+arx_status report(arx_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+}  // namespace arx
+
 extern "C" {
 
 const char* arx_status_string(arx_status s) {

@@ -6,7 +6,15 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "arx.h"
+
 namespace arx {
+
+// Argument checks shared by the C entry points (see abi.cu).
+arx_status validate_io(const void* const* in, int W, const void* out, size_t n, bool* out_alias);
+
+// Sets the calling thread's arx_last_error() text and returns `s`.
+arx_status report(arx_status s, const char* fmt, ...);
 
 // One stateless reduce: out[i] = bf16(sum_r slot[r][i]) for 0 <= i < n.
 struct ReduceCall {

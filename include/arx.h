@@ -17,9 +17,10 @@
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Work is enqueued on it and the call returns without waiting,
  *    except where a function says it synchronises.
- *  - The library allocates no memory, holds no per-call state and owns no
- *    buffer: the caller owns every byte (PyTorch tensors in the Python
- *    binding).  Nothing here takes ownership of a pointer.
+ *  - The library allocates no memory and owns no caller buffer: the caller
+ *    owns every byte (PyTorch tensors in the Python binding), except the one
+ *    static device array behind arx_step_noalloc (below).  Nothing here takes
+ *    ownership of a pointer.
  *  - Errors are returned as arx_status; nothing calls exit() or throws.
  *    Argument errors are detected on the host before anything is enqueued.
  *    arx_last_error() gives a one-line detail for the calling thread.
@@ -197,6 +198,42 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
  * *dev_err = device error word (either pointer may be NULL).  Returns the
  * status in the error word's low 8 bits (ARX_OK when it is 0), or ARX_ECUDA. */
 arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Allocation-free protocol step.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory at the time
+ * they call: a serving engine that reserved nearly all of HBM for its own pool
+ * at start-up, code running while a CUDA graph is captured in global capture
+ * mode (where cudaMalloc is refused), a plug-in whose host framework owns every
+ * allocation, or a latency-critical path that cannot afford the device-wide
+ * synchronisation of cudaMalloc/cudaFree.
+ *
+ * Same operation and result as arx_step, bit for bit, but the workspace is a
+ * static device array inside this library (about 4 MiB: ARX_NOALLOC_MAX_N
+ * elements x ARX_MAX_W ranks x 2 parity banks, plus the protocol words), held
+ * by every GPU that loads the library until the process exits.  Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ *   inputs      HOST array of W device pointers, each to n bf16 elements.
+ *   W           1..ARX_MAX_W virtual ranks.
+ *   out         device pointer to n bf16; may equal one input exactly.
+ *   n           0 < n <= ARX_NOALLOC_MAX_N; larger n returns ARX_EINVAL with
+ *               a message naming the limit (n == 0 returns ARX_OK).
+ *   dev_status  optional DEVICE pointer to one uint32, 4-byte aligned: receives
+ *               the step's device error word (0 = success; layout as for
+ *               arx_step) when the stream reaches it.  NULL skips it.
+ *   stream      cudaStream_t as void*.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call shares the array and
+ * first clears its protocol words, so each call is a fresh protocol instance;
+ * calls that overlap on the GPU (several streams, or unordered host threads)
+ * race on the array and must be serialised by the caller.
+ * ------------------------------------------------------------------------- */
+#define ARX_NOALLOC_MAX_N 131072
+#define ARX_NOALLOC_MAX_BLOCKS 32
+arx_status arx_step_noalloc(const void* const* inputs, int W, void* out, size_t n,
+                            uint32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }
