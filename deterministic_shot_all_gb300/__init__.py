@@ -154,14 +154,22 @@ def arx_reduce_host_staging_bytes(W: int, n: int) -> int:
     return int(lib.arx_reduce_host_staging_bytes(W, n))
 
 
-def arx_reduce_host(host_slots: Sequence, host_out, staging, n: int | None = None,
+def arx_reduce_host(host_slots: Sequence, host_out, staging=None, n: int | None = None,
                     stream=None, check: bool = True) -> int:
-    """Enqueue copy-in, reduce and copy-out for host (ideally pinned) buffers."""
-    nb = staging.numel() * staging.element_size() if hasattr(staging, "numel") else None
-    if nb is None:
-        raise TypeError("staging must be a device tensor")
+    """Enqueue the reduce of host partials into a host output.
+
+    Page-locked buffers are read and written by the kernel directly; pageable
+    ones go through ``staging`` (a device tensor of
+    ``arx_reduce_host_staging_bytes(W, n)`` bytes).
+    """
+    if staging is None:
+        sptr, nb = None, 0
+    elif hasattr(staging, "numel"):
+        sptr, nb = (staging.data_ptr() or None), staging.numel() * staging.element_size()
+    else:
+        raise TypeError("staging must be a device tensor or None")
     st = lib.arx_reduce_host(_ptr_array(host_slots), len(host_slots), _ptr(host_out),
-                             _numel(n, host_out), _ptr(staging), nb, _stream(stream))
+                             _numel(n, host_out), sptr, nb, _stream(stream))
     if check:
         _check(st)
     return st

@@ -123,6 +123,22 @@ size_t arx_reduce_host_staging_bytes(int W, size_t n) {
   return size_t(W) * round_up(n * 2, 256);
 }
 
+namespace {
+
+// Device-usable address of a page-locked (pinned or registered) host buffer,
+// or nullptr if `p` is pageable or unknown to CUDA.
+const void* pinned_device_address(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  return at.devicePointer;
+}
+
+}  // namespace
+
 arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out, size_t n,
                            void* dev_staging, size_t staging_bytes, void* stream) {
   if (n == 0) return ok();
@@ -130,15 +146,38 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
   if (!host_slots || !host_out) return fail(ARX_EINVAL, "null host pointer");
   for (int r = 0; r < W; ++r)
     if (!host_slots[r]) return fail(ARX_EINVAL, "null host slot %d", r);
-  if (!dev_staging) return fail(ARX_EINVAL, "null staging buffer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // Direct form: every buffer page-locked, so the kernel reads the partials
+  // and writes the sum in host memory itself, over the coherent CPU-GPU link
+  // (arx.cu's GB10 design: pinned host buffers are GPU buffers).
+  const void* dev_slots[ARX_MAX_W];
+  bool direct = true;
+  for (int r = 0; r < W && direct; ++r) direct = (dev_slots[r] = pinned_device_address(host_slots[r])) != nullptr;
+  void* dev_out = direct ? const_cast<void*>(pinned_device_address(host_out)) : nullptr;
+  if (direct && dev_out) {
+    bool alias = false;
+    const arx_status s = check_io(dev_slots, W, dev_out, n, &alias);
+    if (s != ARX_OK) return s;
+    arx::ReduceCall c{};
+    for (int r = 0; r < W; ++r) c.slot[r] = static_cast<const uint16_t*>(dev_slots[r]);
+    c.out = static_cast<uint16_t*>(dev_out);
+    c.n = n;
+    c.W = W;
+    c.out_aliases_slot = alias;
+    const cudaError_t e = arx::launch_reduce(c, st);
+    if (e != cudaSuccess) return fail_cuda(e, "arx_reduce_host launch");
+    return ok();
+  }
+
+  // Staged form: one copy in per slot, the reduce in place, one copy out.
+  if (!dev_staging) return fail(ARX_EINVAL, "pageable host buffers need a staging buffer");
   if (reinterpret_cast<uintptr_t>(dev_staging) & 1u) return fail(ARX_EINVAL, "staging not 2-byte aligned");
   const size_t need = arx_reduce_host_staging_bytes(W, n);
   if (need == 0 || staging_bytes < need)
     return fail(ARX_EINVAL, "staging buffer %zu bytes, need %zu", staging_bytes, need);
   const size_t stride = round_up(n * 2, 256);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(dev_staging);
-  const void* dev_slots[ARX_MAX_W];
   for (int r = 0; r < W; ++r) {
     dev_slots[r] = base + size_t(r) * stride;
     const cudaError_t e = cudaMemcpyAsync(base + size_t(r) * stride, host_slots[r], n * 2,

@@ -6,11 +6,21 @@
 // vector.  Each thread reads every slot at a group before it writes that
 // group, so the output may be one of the slots.
 //
-// GB300 design: a persistent grid-stride loop (grid = SMs x resident blocks,
-// capped by the work), U independent groups per thread per iteration so that
-// U*W 16-byte loads are in flight before the first add (Little's law against
-// HBM3e latency), coalesced 512-byte warp accesses per slot, L1 bypassed.
-// The pages' fixed grid of at most 8 blocks and 512 KB cap are dropped.
+// GB300 design (the pages' fixed grid of at most 8 blocks and 512 KB cap are
+// dropped):
+//  * persistent grid-stride loop, grid = SMs x resident blocks (capped by the
+//    work), coalesced 512-byte warp accesses per slot, L1 bypassed;
+//  * U independent groups per thread per iteration, all W*U loads issued
+//    before the first add (Little's law against HBM3e latency);
+//  * software pipelining (kPipe): the next iteration's loads are in flight
+//    while the current groups are summed and stored -- measured best for
+//    small and medium messages and for W <= 4;
+//  * programmatic dependent launch: the kernel waits on its stream
+//    predecessor (griddepcontrol.wait) before touching memory and lets its
+//    successor start launching at once, which hides most of the launch gap
+//    between back-to-back calls.
+// The launch policy (threads, U, kPipe per W and size) comes from a measured
+// sweep of these shapes on GB300.
 #include "arx_device.cuh"
 #include "arx_internal.h"
 
@@ -25,13 +35,6 @@ struct VecArgs {
   size_t groups;   // 16-byte groups after the head
 };
 
-// Independent 16-byte groups per thread per iteration.  W*U vectors are
-// loaded before the first add: 8 vectors (128 B) per thread for every W.
-template <int W>
-struct Unroll {
-  static constexpr int U = W >= 8 ? 1 : (W >= 4 ? 2 : (W >= 2 ? 4 : 8));
-};
-
 template <int W>
 __device__ __forceinline__ void scalar_element(const VecArgs& a, size_t e) {
   float acc = 0.0f;
@@ -40,7 +43,7 @@ __device__ __forceinline__ void scalar_element(const VecArgs& a, size_t e) {
   a.out[e] = round_bf16(acc);
 }
 
-template <int W, bool kAlias>
+template <bool kAlias>
 __device__ __forceinline__ uint4 load_group(const uint4* p) {
   if constexpr (kAlias) {
     return ld_stream(p);
@@ -49,34 +52,74 @@ __device__ __forceinline__ uint4 load_group(const uint4* p) {
   }
 }
 
-template <int W, bool kAlias>
-__global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const VecArgs a) {
-  constexpr int U = Unroll<W>::U;
+// Wait for the previous kernel of the stream (when launched as its
+// programmatic dependent) before any global access, then allow the next one
+// to begin launching; it waits in the same way before touching memory.
+__device__ __forceinline__ void dependent_launch_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+template <int W, int U, bool kAlias>
+__device__ __forceinline__ void load_batch(uint4 (&v)[U][W], const uint4* const (&src)[W], size_t g,
+                                           size_t stride) {
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int r = 0; r < W; ++r) v[u][r] = load_group<kAlias>(src[r] + g + u * stride);
+}
+
+template <int W, int U>
+__device__ __forceinline__ void store_batch(uint4* dst, const uint4 (&v)[U][W], size_t g, size_t stride) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) st_global(dst + g + u * stride, sum_vectors<W>(v[u]));
+}
+
+template <int W, int T, int U, bool kPipe, bool kAlias>
+__global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
+  dependent_launch_prologue();
   const uint4* src[W];
 #pragma unroll
   for (int r = 0; r < W; ++r) src[r] = reinterpret_cast<const uint4*>(a.slot[r] + a.head);
   uint4* dst = reinterpret_cast<uint4*>(a.out + a.head);
 
-  const size_t stride = size_t(gridDim.x) * kThreads;
-  size_t g = size_t(blockIdx.x) * kThreads + threadIdx.x;
+  const size_t stride = size_t(gridDim.x) * T;
+  const size_t step = size_t(U) * stride;
+  size_t g = size_t(blockIdx.x) * T + threadIdx.x;
   const size_t G = a.groups;
 
-  // Main loop: U groups g, g + stride, ..., all loads issued before any add.
-  if (U > 1) {
-    for (; g + size_t(U - 1) * stride < G; g += size_t(U) * stride) {
+  if constexpr (kPipe) {
+    // Batch i+1's loads are issued before batch i is summed and stored.
+    uint4 cur[U][W];
+    bool have = g + size_t(U - 1) * stride < G;
+    if (have) load_batch<W, U, kAlias>(cur, src, g, stride);
+    while (have) {
+      const size_t gn = g + step;
+      const bool more = gn + size_t(U - 1) * stride < G;
+      uint4 nxt[U][W];
+      if (more) load_batch<W, U, kAlias>(nxt, src, gn, stride);
+      store_batch<W, U>(dst, cur, g, stride);
+      g = gn;
+      have = more;
+      if (more) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int r = 0; r < W; ++r) cur[u][r] = nxt[u][r];
+      }
+    }
+  } else if constexpr (U > 1) {
+    for (; g + size_t(U - 1) * stride < G; g += step) {
       uint4 v[U][W];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int r = 0; r < W; ++r) v[u][r] = load_group<W, kAlias>(src[r] + g + u * stride);
-#pragma unroll
-      for (int u = 0; u < U; ++u) st_global(dst + g + u * stride, sum_vectors<W>(v[u]));
+      load_batch<W, U, kAlias>(v, src, g, stride);
+      store_batch<W, U>(dst, v, g, stride);
     }
   }
+  // Remaining groups (fewer than U per thread).
   for (; g < G; g += stride) {
     uint4 v[W];
 #pragma unroll
-    for (int r = 0; r < W; ++r) v[r] = load_group<W, kAlias>(src[r] + g);
+    for (int r = 0; r < W; ++r) v[r] = load_group<kAlias>(src[r] + g);
     st_global(dst + g, sum_vectors<W>(v));
   }
 
@@ -93,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const VecArgs a) {
 // Pointers with different addresses mod 16: one element per thread per step.
 template <int W>
 __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const VecArgs a) {
+  dependent_launch_prologue();
   const size_t stride = size_t(gridDim.x) * kThreads;
   for (size_t e = size_t(blockIdx.x) * kThreads + threadIdx.x; e < a.n; e += stride)
     scalar_element<W>(a, e);
@@ -100,15 +144,65 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const VecArgs a
 
 constexpr int kMaxDevices = 64;
 
-template <int W, bool kAlias>
-int vec_blocks_per_sm(int dev, cudaError_t* err) {
-  static int cache[kMaxDevices];  // 0 = not yet queried
+template <typename Kernel>
+int blocks_per_sm(Kernel k, int threads, int dev, int* cache, cudaError_t* err) {
   if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
   int b = 0;
-  *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reduce_vec_kernel<W, kAlias>, kThreads, 0);
+  *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, threads, 0);
   if (*err != cudaSuccess || b < 1) return -1;
   if (dev >= 0 && dev < kMaxDevices) cache[dev] = b;
   return b;
+}
+
+// Launch with the programmatic-stream-serialisation attribute (see
+// dependent_launch_prologue).
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel k, size_t blocks, int threads, cudaStream_t stream, const VecArgs& a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+  cfg.blockDim = dim3(unsigned(threads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+template <int W, int T, int U, bool kPipe, bool kAlias>
+cudaError_t launch_vec(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
+  static int cache[kMaxDevices];
+  cudaError_t err = cudaSuccess;
+  auto k = reduce_vec_kernel<W, T, U, kPipe, kAlias>;
+  const int per_sm = blocks_per_sm(k, T, dev, cache, &err);
+  if (per_sm < 1) return err;
+  const size_t per_block = size_t(T) * U;
+  size_t blocks = (a.groups + per_block - 1) / per_block;
+  const size_t cap = size_t(sms) * size_t(per_sm);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_dependent(k, blocks, T, stream, a);
+}
+
+// Measured policy (bench.py --sweep and the shape sweep on GB300):
+//  W <= 2: 128 threads, U = 2, pipelined, at every size;
+//  W 3-4:  256 threads, U = 1, pipelined;
+//  W >= 5: 256 threads, U = 1, pipelined up to 2 MiB per partial; above,
+//          U = 2 without pipelining (more loads in flight per thread).
+constexpr size_t kLargePartialElems = size_t(1) << 20;
+
+template <int W, bool kAlias>
+cudaError_t launch_policy(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
+  if constexpr (W <= 2) {
+    return launch_vec<W, 128, 2, true, kAlias>(a, dev, sms, stream);
+  } else if constexpr (W <= 4) {
+    return launch_vec<W, 256, 1, true, kAlias>(a, dev, sms, stream);
+  } else {
+    if (a.n <= kLargePartialElems) return launch_vec<W, 256, 1, true, kAlias>(a, dev, sms, stream);
+    return launch_vec<W, 256, 2, false, kAlias>(a, dev, sms, stream);
+  }
 }
 
 template <int W>
@@ -134,23 +228,16 @@ cudaError_t launch_w(const ReduceCall& c, cudaStream_t stream) {
     if (head > c.n) head = c.n;
     a.head = head;
     a.groups = (c.n - head) / 8u;
-    const int per_sm = c.out_aliases_slot ? vec_blocks_per_sm<W, true>(dev, &err)
-                                          : vec_blocks_per_sm<W, false>(dev, &err);
-    if (per_sm < 1) return err;
-    const size_t per_block = size_t(kThreads) * Unroll<W>::U;
-    size_t blocks = (a.groups + per_block - 1) / per_block;
-    const size_t cap = size_t(sms) * size_t(per_sm);
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    if (c.out_aliases_slot)
-      reduce_vec_kernel<W, true><<<unsigned(blocks), kThreads, 0, stream>>>(a);
-    else
-      reduce_vec_kernel<W, false><<<unsigned(blocks), kThreads, 0, stream>>>(a);
+    err = c.out_aliases_slot ? launch_policy<W, true>(a, dev, sms, stream)
+                             : launch_policy<W, false>(a, dev, sms, stream);
+    if (err != cudaSuccess) return err;
   } else {
     size_t blocks = (c.n + kThreads - 1) / kThreads;
     const size_t cap = size_t(sms) * 8u;
     if (blocks > cap) blocks = cap;
-    reduce_scalar_kernel<W><<<unsigned(blocks), kThreads, 0, stream>>>(a);
+    if (blocks < 1) blocks = 1;
+    err = launch_dependent(reduce_scalar_kernel<W>, blocks, kThreads, stream, a);
+    if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }

@@ -87,23 +87,30 @@ arx_status arx_reduce(const void* const* slots, int W, void* out, size_t n, void
 
 /* ---------------------------------------------------------------------------
  * Host-buffer form of arx_reduce, for callers whose partials live in host
- * memory (the end-to-end form: copies in, reduce, copy out, all enqueued on
- * `stream` in that order).  On arx.cu's GB10 the partials are pinned host
- * buffers the GPU reads directly; here they are copied into device staging.
+ * memory (the end-to-end form: host partials in, host sum out, enqueued on
+ * `stream`).  Same arithmetic and bits as arx_reduce.
+ *
+ * Direct form -- when every host buffer (all slots and host_out) is
+ * page-locked (cudaHostAlloc, cudaHostRegister, torch pin_memory): the reduce
+ * kernel reads the partials and writes the sum in host memory itself, over
+ * GB300's coherent CPU-GPU link, as arx.cu does on GB10 ("pinned host buffers
+ * are GPU buffers").  One kernel, no copies; dev_staging is not used and may
+ * be NULL.
+ * Staged form -- otherwise: one cudaMemcpyAsync per slot into dev_staging,
+ * the reduce in place over staged slot 0, one cudaMemcpyAsync back (copies
+ * from and to pageable memory synchronise with the host).
  *
  *   host_slots     HOST array of W host pointers, each to n bf16 elements.
- *                  Pinned (cudaHostAlloc / page-locked) memory makes the
- *                  copies asynchronous; pageable memory works but the
- *                  copies then synchronise with the host.
- *   host_out       host pointer to n bf16 elements (written when the stream
- *                  reaches the final copy; synchronise `stream` before use).
- *   dev_staging    device buffer of at least arx_reduce_host_staging_bytes(W, n)
- *                  bytes, 256-byte aligned is best; owned by the caller and
- *                  overwritten.  Slot r is staged at byte offset r * stride,
- *                  stride = n*2 rounded up to 256; the sum is written in place
- *                  over staged slot 0 and copied from there.
- * One cudaMemcpyAsync per slot, one kernel, one cudaMemcpyAsync back.
- * Errors as arx_reduce; ARX_EINVAL if the staging buffer is too small.
+ *   host_out       host pointer to n bf16 elements; may equal one slot
+ *                  exactly (written when the stream gets there; synchronise
+ *                  `stream` before reading it, and keep every buffer alive
+ *                  until then).
+ *   dev_staging    staged form only: device buffer of at least
+ *                  arx_reduce_host_staging_bytes(W, n) bytes, owned by the
+ *                  caller and overwritten.  Slot r is staged at byte offset
+ *                  r * stride, stride = n*2 rounded up to 256.
+ * Errors as arx_reduce; ARX_EINVAL if the staged form is needed and the
+ * staging buffer is missing or too small.
  * ------------------------------------------------------------------------- */
 size_t arx_reduce_host_staging_bytes(int W, size_t n);
 arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out, size_t n,

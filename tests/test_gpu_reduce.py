@@ -213,17 +213,46 @@ def test_nondefault_stream_and_graph_capture(arx, dev):
         assert_bits_equal(outs[i].cpu().view(torch.int16).numpy(), want, f"graph call {i}")
 
 
-def test_host_buffer_form(arx, dev):
+def test_host_buffer_form_pinned_direct(arx, dev):
+    # Page-locked buffers: the kernel reads and writes host memory directly.
     W, n = 8, 131072 + 3
     x = sp.partials(W, n, "normal", seed=21)
     want = oracle.reduce(list(sp.to_u16_numpy(x)))
     host = [x[r].clone().pin_memory() for r in range(W)]
     hout = torch.empty(n, dtype=torch.bfloat16).pin_memory()
-    staging = torch.empty(arx.arx_reduce_host_staging_bytes(W, n), dtype=torch.uint8, device=dev)
     for _ in range(2):
         hout.zero_()
-        arx.arx_reduce_host(host, hout, staging)
+        lib_rc = arx.lib.arx_reduce_host(arx._ptr_array(host), W, hout.data_ptr(), n, None, 0,
+                                         torch.cuda.current_stream().cuda_stream)
+        assert lib_rc == arx.ARX_OK, arx.arx_last_error()   # no staging needed
         torch.cuda.current_stream().synchronize()
-        assert_bits_equal(hout.view(torch.int16).numpy(), want, "host form")
+        assert_bits_equal(hout.view(torch.int16).numpy(), want, "pinned direct")
+    for r in range(W):
+        assert torch.equal(host[r].view(torch.int16), x[r].view(torch.int16))
+
+
+def test_host_buffer_form_pinned_in_place(arx, dev):
+    W, n = 4, 50001
+    x = sp.partials(W, n, "normal0.02", seed=22)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    host = [x[r].clone().pin_memory() for r in range(W)]
+    arx.arx_reduce_host(host, host[0], torch.empty(0, dtype=torch.uint8, device=dev))
+    torch.cuda.current_stream().synchronize()
+    assert_bits_equal(host[0].view(torch.int16).numpy(), want, "pinned in place")
+
+
+def test_host_buffer_form_pageable_staged(arx, dev):
+    W, n = 3, 70001
+    x = sp.partials(W, n, "special", seed=23)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    host = [x[r].clone() for r in range(W)]                  # pageable
+    hout = torch.zeros(n, dtype=torch.bfloat16)
+    staging = torch.empty(arx.arx_reduce_host_staging_bytes(W, n), dtype=torch.uint8, device=dev)
+    arx.arx_reduce_host(host, hout, staging)
+    torch.cuda.current_stream().synchronize()
+    assert_bits_equal(hout.view(torch.int16).numpy(), want, "pageable staged")
     small = torch.empty(arx.arx_reduce_host_staging_bytes(W, n) - 2, dtype=torch.uint8, device=dev)
     assert arx.arx_reduce_host(host, hout, small, check=False) == arx.ARX_EINVAL
+    rc = arx.lib.arx_reduce_host(arx._ptr_array(host), W, hout.data_ptr(), n, None, 0,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == arx.ARX_EINVAL and "staging" in arx.arx_last_error()
