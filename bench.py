@@ -359,6 +359,7 @@ def run_native(args) -> None:
 
     extra = {}
     if not args.quick:
+        extra["latency_floor"] = floor_point(torch, arx, dev, stream, l2, W, n, per_call)
         extra["bandwidth"] = bandwidth_points(torch, arx, sp, dev, stream, l2)
         extra["protocol"] = protocol_point(torch, arx, sp, dev, stream, l2, args.workload)
         extra["e2e"] = e2e_point(torch, arx, sp, dev, stream, args.workload, max(200, min(args.steps, 5000)), l2)
@@ -430,6 +431,29 @@ def bandwidth_points(torch, arx, sp, dev, stream, l2) -> list:
         del parts, outs, slot_lists
         torch.cuda.empty_cache()
     return pts
+
+
+def floor_point(torch, arx, dev, stream, l2, W, n, per_call) -> dict:
+    """Per-call floor: the same call shape with 1 KiB partials (launch + one DRAM round trip).
+
+    The headline message is latency-bound; its time above this floor is what
+    its bytes cost, so bytes / (t - floor) is the marginal bandwidth.
+    """
+    n0 = 512
+    R = rotation_sets((W + 1) * n0 * 2, l2, cap=4096)
+    parts = torch.zeros(R, W, n0, dtype=torch.bfloat16, device=dev)
+    outs = torch.empty(R, n0, dtype=torch.bfloat16, device=dev)
+    lists = [[parts[k, r] for r in range(W)] for k in range(R)]
+
+    def call(i):
+        arx.arx_reduce(lists[i % R], outs[i % R], stream=stream)
+
+    calls = 20000
+    t = timed_graph_calls(torch, stream, call, calls, 100)
+    floor = t / calls
+    above = per_call - floor
+    return {"n": n0, "us_per_call": floor * 1e6, "headline_us_above_floor": above * 1e6,
+            "marginal_GBs": gbs((W + 1) * n * 2, above) if above > 0 else None}
 
 
 def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:

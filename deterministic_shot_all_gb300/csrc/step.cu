@@ -40,6 +40,9 @@ constexpr uint32_t kErrState = 5;
 
 enum Stage : uint32_t { kStartWait = 1, kEndWait = 2, kPadSend = 3, kPadWait = 4, kEpoch = 5 };
 
+// 16-byte vectors each thread loads before storing them while staging.
+constexpr int kStageBatch = 4;
+
 struct Header {  // first bytes of the workspace
   uint32_t seq;        // completed steps
   uint32_t err;        // device error word
@@ -153,23 +156,28 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     const uint16_t* in = a.in[r];
     uint16_t* dst = bank + size_t(r) * stride;
     if ((a.in_vec_mask >> r) & 1u) {
+      // Batches of kStageBatch vectors per thread: every load of a batch is
+      // in flight before the first store.
       const uint4* s4 = reinterpret_cast<const uint4*>(in);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
-      for (size_t g = c0 + tid; g < c1; g += kThreads) st_global(d4 + g, ld_stream(s4 + g));
+      for (size_t g0 = c0 + tid; g0 < c1; g0 += size_t(kStageBatch) * kThreads) {
+        uint4 v[kStageBatch];
+#pragma unroll
+        for (int k = 0; k < kStageBatch; ++k) {
+          const size_t g = g0 + size_t(k) * kThreads;
+          if (g < c1) v[k] = ld_stream(s4 + g);
+        }
+#pragma unroll
+        for (int k = 0; k < kStageBatch; ++k) {
+          const size_t g = g0 + size_t(k) * kThreads;
+          if (g < c1) st_global(d4 + g, v[k]);
+        }
+      }
     } else {
       for (size_t e = 8u * c0 + tid; e < 8u * c1; e += kThreads) dst[e] = in[e];
     }
     if (b == B - 1u && tid < tail) dst[8u * G + tid] = in[8u * G + tid];
   }
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {  // last block publishes
-      hdr->blocks[0] = 0u;
-      st_relaxed_gpu(&hdr->published, seq);
-    }
-  }
-
   // 4. end barrier, fenced: every thread's staging precedes the release.
   __syncthreads();
   if (lane == 0 && warp < uint32_t(W)) {
@@ -184,6 +192,14 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       } else {
         record_error(&hdr->err, kErrTimeout, kEndWait, r, b);
       }
+    }
+  } else if (tid == 1) {
+    // Last block past the copy publishes seq.  Done by a thread that neither
+    // signals nor waits, so it overlaps the barrier instead of preceding it.
+    __threadfence();
+    if (atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
+      hdr->blocks[0] = 0u;
+      st_relaxed_gpu(&hdr->published, seq);
     }
   }
   __syncthreads();
@@ -227,9 +243,15 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   __syncthreads();
   if (tid < uint32_t(W)) {
     const uint32_t t = tid;
-    if (!cas_until(&pad[(t * B + b) * uint32_t(W) + r], 0u, 1u, a.timeout_ns))
+    uint32_t* send = &pad[(t * B + b) * uint32_t(W) + r];
+    uint32_t* recv = &pad[(r * B + b) * uint32_t(W) + t];
+    // First attempts of the send (0 -> 1) and the wait (1 -> 0) go out back to
+    // back; only a failed attempt is retried, within the bound.
+    const uint32_t sent = atom_cas_relaxed_gpu(send, 0u, 1u);
+    const uint32_t got = atom_cas_relaxed_gpu(recv, 1u, 0u);
+    if (sent != 0u && !cas_until(send, 0u, 1u, a.timeout_ns))
       record_error(&hdr->err, kErrTimeout, kPadSend, r, b);
-    if (!cas_until(&pad[(r * B + b) * uint32_t(W) + t], 1u, 0u, a.timeout_ns))
+    if (got != 1u && !cas_until(recv, 1u, 0u, a.timeout_ns))
       record_error(&hdr->err, kErrTimeout, kPadWait, r, b);
   }
   __syncthreads();
