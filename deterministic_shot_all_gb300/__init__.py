@@ -14,8 +14,9 @@ Functions keep the C names:
 * ``arx_reduce_host(host_slots, host_out, staging)``: the same from and to
   host buffers, copies included.
 * ``arx_ctx_workspace_bytes / arx_ctx_init / arx_step / arx_ctx_query /
-  arx_ctx_reset / arx_ctx_set_timeout / arx_ctx_set_fault``: the seq/parity
-  protocol step with Semaphore epochs and a zero-resetting signal pad.
+  arx_ctx_reset / arx_ctx_set_timeout / arx_ctx_set_fault / arx_ctx_set_sync``:
+  the seq/parity protocol step with Semaphore epochs and a zero-resetting
+  signal pad, in three barrier variants.
 """
 
 from __future__ import annotations
@@ -32,6 +33,7 @@ ARX_MAX_W = 8
 ARX_STEP_MAX_BLOCKS = 256
 ARX_DEFAULT_TIMEOUT_NS = 1_000_000_000
 ARX_NOALLOC_MAX_N = 131072
+ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED = range(3)
 
 
 class ArxError(RuntimeError):
@@ -47,6 +49,8 @@ class arx_ctx(ctypes.Structure):
         ("W", ctypes.c_int32),
         ("nblocks", ctypes.c_int32),
         ("fault_rank", ctypes.c_int32),
+        ("sync_mode", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
         ("max_n", ctypes.c_uint64),
         ("slot_stride", ctypes.c_uint64),
         ("timeout_ns", ctypes.c_uint64),
@@ -79,6 +83,7 @@ def _load() -> ctypes.CDLL:
         "arx_ctx_init": ([ctxp, vp, sz, i32, sz, i32], i32),
         "arx_ctx_set_timeout": ([ctxp, u64], i32),
         "arx_ctx_set_fault": ([ctxp, i32], i32),
+        "arx_ctx_set_sync": ([ctxp, i32], i32),
         "arx_ctx_reset": ([ctxp, vp], i32),
         "arx_step": ([ctxp, ptrs, vp, sz, vp], i32),
         "arx_ctx_query": ([ctxp, u32p, u32p, vp], i32),
@@ -193,6 +198,11 @@ def arx_ctx_set_timeout(ctx: arx_ctx, ns: int) -> None:
     _check(lib.arx_ctx_set_timeout(ctypes.byref(ctx), int(ns)))
 
 
+def arx_ctx_set_sync(ctx: arx_ctx, mode: int) -> None:
+    """Barrier variant of later steps: ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD or ARX_SYNC_PAD_FENCED."""
+    _check(lib.arx_ctx_set_sync(ctypes.byref(ctx), int(mode)))
+
+
 def arx_ctx_set_fault(ctx: arx_ctx, rank: int) -> None:
     _check(lib.arx_ctx_set_fault(ctypes.byref(ctx), int(rank)))
 
@@ -235,6 +245,6 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
 __all__ = [
     "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce",
     "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
-    "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_reset", "arx_step", "arx_ctx_query",
+    "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_set_sync", "arx_ctx_reset", "arx_step", "arx_ctx_query",
     "arx_step_noalloc",
 ]

@@ -276,6 +276,7 @@ arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t m
   ctx->W = W;
   ctx->nblocks = B;
   ctx->fault_rank = -1;
+  ctx->sync_mode = ARX_SYNC_SEMAPHORE;
   ctx->max_n = max_n;
   ctx->slot_stride = L.slot_stride;
   ctx->timeout_ns = ARX_DEFAULT_TIMEOUT_NS;
@@ -294,6 +295,15 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns) {
   if (s != ARX_OK) return s;
   if (ns == 0) return fail(ARX_EINVAL, "timeout must be > 0");
   ctx->timeout_ns = ns;
+  return ok();
+}
+
+arx_status arx_ctx_set_sync(arx_ctx* ctx, int mode) {
+  const arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  if (mode != ARX_SYNC_SEMAPHORE && mode != ARX_SYNC_PAD && mode != ARX_SYNC_PAD_FENCED)
+    return fail(ARX_EINVAL, "unknown sync mode %d", mode);
+  ctx->sync_mode = mode;
   return ok();
 }
 
@@ -319,6 +329,8 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   if (n == 0) return ok();
   if (n > ctx->max_n) return fail(ARX_EINVAL, "n=%zu exceeds the context's max_n=%llu", n,
                                   static_cast<unsigned long long>(ctx->max_n));
+  if (ctx->sync_mode < ARX_SYNC_SEMAPHORE || ctx->sync_mode > ARX_SYNC_PAD_FENCED)
+    return fail(ARX_ESTATE, "context holds an unknown sync mode %d", ctx->sync_mode);
   bool alias = false;
   s = check_io(inputs, ctx->W, out, n, &alias);
   if (s != ARX_OK) return s;
@@ -344,6 +356,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.W = ctx->W;
   c.B = ctx->nblocks;
   c.fault_rank = ctx->fault_rank;
+  c.sync_mode = ctx->sync_mode;
   e = arx::launch_step(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_step launch");
   return ok();

@@ -68,6 +68,22 @@ __device__ __forceinline__ uint4 sum_vectors(const uint4 (&v)[W]) {
   return pack8(acc);
 }
 
+// The same for 8-byte vectors of 4 bf16.
+__device__ __forceinline__ void accumulate4(float (&acc)[4], const uint2& v) {
+  acc[0] = __fadd_rn(acc[0], widen_lo(v.x));
+  acc[1] = __fadd_rn(acc[1], widen_hi(v.x));
+  acc[2] = __fadd_rn(acc[2], widen_lo(v.y));
+  acc[3] = __fadd_rn(acc[3], widen_hi(v.y));
+}
+
+template <int W>
+__device__ __forceinline__ uint2 sum_halves(const uint2 (&v)[W]) {
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int r = 0; r < W; ++r) accumulate4(acc, v[r]);
+  return make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+}
+
 // ---- 16-byte global loads and stores --------------------------------------------
 
 // Read-only streaming load: non-coherent path, no L1 allocation.  Only for
@@ -108,6 +124,24 @@ __device__ __forceinline__ void st_global(uint4* p, const uint4& v) {
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// 8-byte forms of the streaming loads and the store.
+__device__ __forceinline__ uint2 ld_stream_nc(const uint2* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream(const uint2* p) {
+  uint2 v;
+  asm volatile("ld.global.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_global(uint2* p, const uint2& v) {
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // ---- scoped atomics and loads for the protocol words (one GPU: .gpu scope) -------
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -141,6 +175,20 @@ __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v
 __device__ __forceinline__ uint32_t atom_cas_relaxed_gpu(uint32_t* p, uint32_t cmp, uint32_t val) {
   uint32_t old;
   asm volatile("atom.relaxed.gpu.global.cas.b32 %0, [%1], %2, %3;"
+               : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t atom_cas_release_gpu(uint32_t* p, uint32_t cmp, uint32_t val) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.cas.b32 %0, [%1], %2, %3;"
+               : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t atom_cas_acquire_gpu(uint32_t* p, uint32_t cmp, uint32_t val) {
+  uint32_t old;
+  asm volatile("atom.acquire.gpu.global.cas.b32 %0, [%1], %2, %3;"
                : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
   return old;
 }

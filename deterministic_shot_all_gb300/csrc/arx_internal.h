@@ -39,6 +39,7 @@ struct StepCall {
   uint64_t timeout_ns;
   int W, B;
   int fault_rank;
+  int sync_mode;  // ARX_SYNC_*
 };
 
 cudaError_t launch_step(const StepCall& c, cudaStream_t stream);

@@ -24,6 +24,20 @@
 //     the last block out resets the second counter and stores seq as
 //     completed (arx.cu "last block out").
 //
+// Barrier variants (the context's sync mode), all with the same data path:
+//  * Semaphore (default): steps 2 and 4 as above, step 6 a relaxed pad barrier.
+//  * Pad: every barrier is triton_barrier.py's `blockwise_barrier` on the
+//    signal pad, in the page's three patterns -- Pattern 0 at the start
+//    (relaxed barrier, then block sync), Pattern 1 after staging (block sync,
+//    acq_rel barrier, block sync) and Pattern 2 at exit.  The Semaphores are
+//    not touched.
+//  * Pad, fenced: as Pad, but all three barriers use acq_rel compare-and-swaps
+//    (the page's "acq_rel" sem everywhere instead of "relaxed" where its
+//    patterns allow it).
+// One pad serves all three barriers of a step: a send spins until the
+// receiver has consumed the previous signal (the word is back at 0), so
+// consecutive barriers pair their sends and waits in order.
+//
 // Every wait is bounded by the context's timeout (global timer plus a spin
 // cap): on expiry the block records ARX_ETIMEOUT with its stage, rank and
 // block in the error word and carries on, so the kernel always finishes and
@@ -38,7 +52,13 @@ namespace {
 constexpr uint32_t kErrTimeout = 4;
 constexpr uint32_t kErrState = 5;
 
-enum Stage : uint32_t { kStartWait = 1, kEndWait = 2, kPadSend = 3, kPadWait = 4, kEpoch = 5 };
+enum Stage : uint32_t {
+  kStartWait = 1, kEndWait = 2, kPadSend = 3, kPadWait = 4, kEpoch = 5,
+  kStartPadSend = 6, kStartPadWait = 7, kEndPadSend = 8, kEndPadWait = 9
+};
+
+// Barrier variants (arx.h, ARX_SYNC_*).
+enum SyncMode : int { kSyncSemaphore = 0, kSyncPad = 1, kSyncPadFenced = 2 };
 
 // 16-byte vectors each thread loads before storing them while staging.
 constexpr int kStageBatch = 4;
@@ -106,12 +126,62 @@ __device__ bool cas_until(uint32_t* p, uint32_t from, uint32_t to, uint64_t time
   }
 }
 
+// Compare-and-swap `from -> to` until it succeeds, bounded, with acquire or
+// release semantics (the "acq_rel" sem of triton_barrier.py).
+template <bool kRelease>
+__device__ __forceinline__ uint32_t cas_ordered(uint32_t* p, uint32_t from, uint32_t to) {
+  return kRelease ? atom_cas_release_gpu(p, from, to) : atom_cas_acquire_gpu(p, from, to);
+}
+
+template <bool kRelease>
+__device__ bool cas_until_ordered(uint32_t* p, uint32_t from, uint32_t to, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  const uint64_t cap = spin_cap(timeout_ns);
+  for (uint64_t spins = 0;; ++spins) {
+    if (cas_ordered<kRelease>(p, from, to) == from) return true;
+    if ((spins & 15u) == 15u) {
+      if (global_timer_ns() - t0 > timeout_ns || spins > cap) return false;
+      backoff(spins);
+    }
+  }
+}
+
+// triton_barrier.py `blockwise_barrier` for block b of virtual rank r, run by
+// thread t < W: send_signal to pad[t][b][r] (0 -> 1) and wait_signal on
+// pad[r][b][t] (1 -> 0), which leaves the pad all zero once every block of
+// the barrier has passed.  kAcqRel: release send and acquire wait (the page's
+// "acq_rel" sem; a fence first makes the whole block's earlier writes part of
+// the release); otherwise relaxed.  The first send and wait attempts go out
+// back to back; only a failed attempt is retried, within the bound.
+// `send` false skips the send (fault injection).
+template <bool kAcqRel>
+__device__ void pad_barrier(uint32_t* pad, uint32_t B, uint32_t W, uint32_t b, uint32_t r, uint32_t t,
+                            bool send, uint64_t timeout_ns, uint32_t* err, uint32_t stage_send,
+                            uint32_t stage_wait) {
+  uint32_t* to = &pad[(t * B + b) * W + r];
+  uint32_t* from = &pad[(r * B + b) * W + t];
+  if constexpr (kAcqRel) __threadfence();
+  const uint32_t sent = send ? (kAcqRel ? atom_cas_release_gpu(to, 0u, 1u) : atom_cas_relaxed_gpu(to, 0u, 1u)) : 0u;
+  const uint32_t got = kAcqRel ? atom_cas_acquire_gpu(from, 1u, 0u) : atom_cas_relaxed_gpu(from, 1u, 0u);
+  if (send && sent != 0u) {
+    const bool ok = kAcqRel ? cas_until_ordered<true>(to, 0u, 1u, timeout_ns) : cas_until(to, 0u, 1u, timeout_ns);
+    if (!ok) record_error(err, kErrTimeout, stage_send, r, b);
+  }
+  if (got != 1u) {
+    const bool ok = kAcqRel ? cas_until_ordered<false>(from, 1u, 0u, timeout_ns) : cas_until(from, 1u, 0u, timeout_ns);
+    if (!ok) record_error(err, kErrTimeout, stage_wait, r, b);
+  }
+  if constexpr (kAcqRel) __threadfence();
+}
+
 __device__ __forceinline__ size_t split_point(size_t total, uint32_t parts, uint32_t i) {
   return total / parts * i + (total % parts) * i / parts;
 }
 
-template <int W>
+template <int W, int kSync>
 __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
+  constexpr bool kPad = kSync != kSyncSemaphore;
+  constexpr bool kFencedAll = kSync == kSyncPadFenced;
   const uint32_t b = blockIdx.x, r = blockIdx.y;
   const uint32_t B = uint32_t(a.B);
   const uint32_t tid = threadIdx.x, warp = tid / 32u, lane = tid % 32u;
@@ -131,16 +201,24 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     if (epoch[r * B + b] != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
 
-  // 2. start barrier, unfenced: no block barrier before the signal.
+  // 2. start barrier.
   Semaphore& own = sem[r * B + b];
   uint32_t base = 0;
-  if (lane == 0 && warp < uint32_t(W)) {
-    atom_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
-    if (warp == r) {
-      base = own.counter;
-      if (!semaphore_wait<false>(&own.flag, base, uint32_t(W), a.timeout_ns))
-        record_error(&hdr->err, kErrTimeout, kStartWait, r, b);
+  if constexpr (!kPad) {
+    // PullController start stage, unfenced: no block barrier before the signal.
+    if (lane == 0 && warp < uint32_t(W)) {
+      atom_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
+      if (warp == r) {
+        base = own.counter;
+        if (!semaphore_wait<false>(&own.flag, base, uint32_t(W), a.timeout_ns))
+          record_error(&hdr->err, kErrTimeout, kStartWait, r, b);
+      }
     }
+  } else {
+    // Pattern 0: the barrier, then the block synchronises.
+    if (tid < uint32_t(W))
+      pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err,
+                              kStartPadSend, kStartPadWait);
   }
   __syncthreads();
   const uint32_t seq = s_seq;
@@ -180,7 +258,20 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   }
   // 4. end barrier, fenced: every thread's staging precedes the release.
   __syncthreads();
-  if (lane == 0 && warp < uint32_t(W)) {
+  if constexpr (kPad) {
+    // Pattern 1: block sync, acq_rel barrier, block sync.
+    if (tid < uint32_t(W)) {
+      pad_barrier<true>(pad, B, uint32_t(W), b, r, tid, int(r) != a.fault_rank, a.timeout_ns, &hdr->err,
+                        kEndPadSend, kEndPadWait);
+    } else if (tid == 32u) {
+      // Last block past the copy publishes seq (a thread outside the barrier).
+      __threadfence();
+      if (atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
+        hdr->blocks[0] = 0u;
+        st_relaxed_gpu(&hdr->published, seq);
+      }
+    }
+  } else if (lane == 0 && warp < uint32_t(W)) {
     if (int(r) != a.fault_rank) {
       __threadfence();
       atom_add_release_gpu(&sem[warp * B + b].flag, 1u);
@@ -239,21 +330,12 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     }
   }
 
-  // 6. exit: zero-resetting pad barrier (Pattern 2: block barrier, then relaxed).
+  // 6. exit: zero-resetting pad barrier (Pattern 2: block barrier, then the
+  // barrier -- relaxed, or acq_rel in the fenced variant).
   __syncthreads();
-  if (tid < uint32_t(W)) {
-    const uint32_t t = tid;
-    uint32_t* send = &pad[(t * B + b) * uint32_t(W) + r];
-    uint32_t* recv = &pad[(r * B + b) * uint32_t(W) + t];
-    // First attempts of the send (0 -> 1) and the wait (1 -> 0) go out back to
-    // back; only a failed attempt is retried, within the bound.
-    const uint32_t sent = atom_cas_relaxed_gpu(send, 0u, 1u);
-    const uint32_t got = atom_cas_relaxed_gpu(recv, 1u, 0u);
-    if (sent != 0u && !cas_until(send, 0u, 1u, a.timeout_ns))
-      record_error(&hdr->err, kErrTimeout, kPadSend, r, b);
-    if (got != 1u && !cas_until(recv, 1u, 0u, a.timeout_ns))
-      record_error(&hdr->err, kErrTimeout, kPadWait, r, b);
-  }
+  if (tid < uint32_t(W))
+    pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
+                            kPadWait);
   __syncthreads();
   if (tid == 0) {
     epoch[r * B + b] = (epoch[r * B + b] + 1u) % 2u;  // PushController::exit
@@ -268,15 +350,24 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 
 constexpr int kMaxDevices = 64;
 
+// Resident blocks per SM of the step kernel for W ranks: the least over the
+// sync modes, so one capacity serves every mode.
 template <int W>
 int blocks_per_sm(int dev, cudaError_t* err) {
   static int cache[kMaxDevices];
   if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
-  int b = 0;
-  *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, step_kernel<W>, kThreads, 0);
-  if (*err != cudaSuccess || b < 1) return -1;
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = b;
-  return b;
+  int lo = 0;
+  const void* kernels[3] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncPad>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced>)};
+  for (const void* k : kernels) {
+    int b = 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, 0);
+    if (*err != cudaSuccess || b < 1) return -1;
+    lo = lo == 0 || b < lo ? b : lo;
+  }
+  if (dev >= 0 && dev < kMaxDevices) cache[dev] = lo;
+  return lo;
 }
 
 template <int W>
@@ -310,7 +401,13 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, step_kernel<W>, a);
+  cudaError_t err = cudaErrorInvalidValue;
+  switch (c.sync_mode) {
+    case kSyncSemaphore: err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore>, a); break;
+    case kSyncPad: err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPad>, a); break;
+    case kSyncPadFenced: err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPadFenced>, a); break;
+    default: break;
+  }
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

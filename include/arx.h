@@ -151,14 +151,18 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  *   off_pad         uint32 pad[W][B][W], pad[owner][b][sender]  (signal pad)
  *   off_slots       bf16 slots[2][W][slot_stride]         (parity x rank)
  * Device error word: low 8 bits an arx_status, bits 8-11 the stage that
- * failed (1 start wait, 2 end wait, 3 pad send, 4 pad wait, 5 epoch check),
- * bits 12-15 the virtual rank, bits 16-31 the block.
+ * failed (1 start Semaphore wait, 2 end Semaphore wait, 3 exit pad send,
+ * 4 exit pad wait, 5 epoch check, 6 start pad send, 7 start pad wait, 8 end
+ * pad send, 9 end pad wait), bits 12-15 the virtual rank, bits 16-31 the
+ * block.
  * ------------------------------------------------------------------------- */
 typedef struct arx_ctx {
   uint32_t magic;        /* set by arx_ctx_init */
   int32_t W;             /* virtual ranks, 1..ARX_MAX_W */
   int32_t nblocks;       /* B, thread blocks per virtual rank */
   int32_t fault_rank;    /* -1, or a virtual rank that skips its end-barrier signal (testing) */
+  int32_t sync_mode;     /* ARX_SYNC_* (arx_ctx_set_sync); ARX_SYNC_SEMAPHORE after init */
+  int32_t reserved0;
   uint64_t max_n;        /* capacity of one slot, elements */
   uint64_t slot_stride;  /* elements from one slot to the next (multiple of 128) */
   uint64_t timeout_ns;   /* bound of every device wait */
@@ -182,6 +186,29 @@ arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t m
 
 /* Sets the bound of every device wait (ns > 0). */
 arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
+
+/* Barrier variants of the step (same data path and result; they differ in
+ * which of the pages' barriers run and in their memory ordering):
+ *  ARX_SYNC_SEMAPHORE   common.cuh's PullController over the Semaphores for
+ *                       the start (unfenced) and end (fenced: release adds,
+ *                       acquire waits) barriers; triton_barrier.py's
+ *                       blockwise_barrier, Pattern 2, relaxed, at exit.
+ *  ARX_SYNC_PAD         triton_barrier.py's blockwise_barrier on the signal
+ *                       pad for all three: Pattern 0 (relaxed) at the start,
+ *                       Pattern 1 (acq_rel) after staging, Pattern 2
+ *                       (relaxed) at exit.  The Semaphores stay untouched.
+ *  ARX_SYNC_PAD_FENCED  as ARX_SYNC_PAD with acq_rel compare-and-swaps in all
+ *                       three barriers.
+ * After every completed step the pad is all zero in every mode; in the pad
+ * modes the Semaphore flags and counters keep their values. */
+#define ARX_SYNC_SEMAPHORE 0
+#define ARX_SYNC_PAD 1
+#define ARX_SYNC_PAD_FENCED 2
+
+/* Selects the barrier variant of later steps (ARX_EINVAL for an unknown
+ * mode).  Switching between steps is allowed: every mode leaves the pad all
+ * zero and reads the Semaphores only as its own barriers wrote them. */
+arx_status arx_ctx_set_sync(arx_ctx* ctx, int mode);
 
 /* Testing knob: virtual rank `rank` (0..W-1) skips its end-barrier signal, so
  * the step's waits expire and report ARX_ETIMEOUT; -1 turns it off.  No GPU

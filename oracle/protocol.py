@@ -38,6 +38,17 @@ Phases of one step, with the passage each follows:
    resets the second block counter and records ``seq`` as completed
    (arx.cu, "last block out").
 
+Barrier variants (``sync``), with the same data path:
+
+* ``"semaphore"`` -- the phases above.
+* ``"pad"`` -- every barrier is triton_barrier.py's ``blockwise_barrier`` on
+  the signal pad, in its three patterns: Pattern 0 for the start barrier,
+  Pattern 1 (acq_rel) for the end barrier, Pattern 2 at exit.  The
+  Semaphore flags and counters are not touched.
+* ``"pad_fenced"`` -- as ``"pad"``; only the memory ordering of the start and
+  exit barriers differs (acq_rel), which a sequential model does not see, so
+  the words after a step are the same as for ``"pad"``.
+
 All protocol words are unsigned 32-bit and wrap modulo 2**32, as the pages'
 ``uint32_t`` flags do (``flag - base`` in ``PullController::sync`` is an
 unsigned difference).
@@ -92,52 +103,19 @@ def _set_err(st: State, code: int) -> None:
         st.err = code
 
 
-def step(st: State, inputs, skip_end_signal_rank: int | None = None) -> np.ndarray:
-    """Run one protocol step on ``st`` in place; return the bf16 output patterns.
+SYNC_MODES = ("semaphore", "pad", "pad_fenced")
 
-    ``inputs`` is a sequence of W uint16 arrays of equal length.
-    ``skip_end_signal_rank`` models a virtual rank that never sends its
-    end-barrier signal (the host-side fault injection): every wait of that
-    barrier then expires and the error word reports ETIMEOUT.
-    """
+
+def _pad_barrier(st: State, skip_rank: int | None = None) -> None:
+    """triton_barrier.py ``blockwise_barrier`` for every block: rank r sends to
+    ``pad[t][b][r]`` (0 -> 1) for every t, then waits on ``pad[r][b][t]``
+    (1 -> 0) for every t.  A rank in ``skip_rank`` sends nothing, so the waits
+    on its words expire (ETIMEOUT) and leave them at 0."""
     W, B = st.W, st.B
-    if len(inputs) != W:
-        raise ValueError("need one input per virtual rank")
-    inputs = [np.ascontiguousarray(np.asarray(x, dtype=np.uint16)).reshape(-1) for x in inputs]
-
-    # 1. seq / parity, and the per-block epoch check.
-    seq = (st.seq + 1) & MASK32
-    par = seq & 1
-    expect_epoch = (seq - 1) & 1
-    if np.any(st.epoch != expect_epoch):
-        _set_err(st, ESTATE)
-
-    # 2. start barrier (unfenced): one add per rank, wait for W.
-    st.flag = (st.flag + W) & MASK32
-    ok = ((st.flag - st.counter) & MASK32) >= W
-    if not ok.all():
-        _set_err(st, ETIMEOUT)
-
-    # 3. stage rank r's input into slots[par][r]; last block publishes seq.
-    for r in range(W):
-        st.slots[par][r] = inputs[r].copy()
-    st.blocks[0] = 0
-    st.published = seq
-
-    # 4. end barrier (fenced): one add per sending rank, wait for 2W, advance counter.
-    senders = W - (1 if skip_end_signal_rank is not None else 0)
-    st.flag = (st.flag + senders) & MASK32
-    reached = ((st.flag - st.counter) & MASK32) >= 2 * W
-    if not reached.all():
-        _set_err(st, ETIMEOUT)
-    st.counter = np.where(reached, (st.counter + 2 * W) & MASK32, st.counter)
-
-    # 5. rank-order reduce of the staged slots.
-    out = _reduce([st.slots[par][r] for r in range(W)])
-
-    # 6. exit: zero-resetting pad barrier, epoch flip, last block out.
     for b in range(B):
         for r in range(W):          # sends: 0 -> 1
+            if r == skip_rank:
+                continue
             for t in range(W):
                 if st.pad[t, b, r] != 0:
                     _set_err(st, ETIMEOUT)
@@ -147,6 +125,66 @@ def step(st: State, inputs, skip_end_signal_rank: int | None = None) -> np.ndarr
                 if st.pad[r, b, t] != 1:
                     _set_err(st, ETIMEOUT)
                 st.pad[r, b, t] = 0
+
+
+def step(st: State, inputs, skip_end_signal_rank: int | None = None,
+         sync: str = "semaphore") -> np.ndarray:
+    """Run one protocol step on ``st`` in place; return the bf16 output patterns.
+
+    ``inputs`` is a sequence of W uint16 arrays of equal length.
+    ``skip_end_signal_rank`` models a virtual rank that never sends its
+    end-barrier signal (the host-side fault injection): every wait of that
+    barrier then expires and the error word reports ETIMEOUT.  ``sync`` is
+    the barrier variant (``SYNC_MODES``).
+    """
+    W, B = st.W, st.B
+    if len(inputs) != W:
+        raise ValueError("need one input per virtual rank")
+    if sync not in SYNC_MODES:
+        raise ValueError(f"unknown sync mode {sync!r}")
+    pad_mode = sync != "semaphore"
+    inputs = [np.ascontiguousarray(np.asarray(x, dtype=np.uint16)).reshape(-1) for x in inputs]
+
+    # 1. seq / parity, and the per-block epoch check.
+    seq = (st.seq + 1) & MASK32
+    par = seq & 1
+    expect_epoch = (seq - 1) & 1
+    if np.any(st.epoch != expect_epoch):
+        _set_err(st, ESTATE)
+
+    # 2. start barrier: Semaphore start stage (unfenced): one add per rank,
+    # wait for W -- or Pattern 0 of the pad barrier.
+    if pad_mode:
+        _pad_barrier(st)
+    else:
+        st.flag = (st.flag + W) & MASK32
+        ok = ((st.flag - st.counter) & MASK32) >= W
+        if not ok.all():
+            _set_err(st, ETIMEOUT)
+
+    # 3. stage rank r's input into slots[par][r]; last block publishes seq.
+    for r in range(W):
+        st.slots[par][r] = inputs[r].copy()
+    st.blocks[0] = 0
+    st.published = seq
+
+    # 4. end barrier (fenced): Semaphore end stage -- one add per sending rank,
+    # wait for 2W, advance counter -- or Pattern 1 of the pad barrier.
+    if pad_mode:
+        _pad_barrier(st, skip_end_signal_rank)
+    else:
+        senders = W - (1 if skip_end_signal_rank is not None else 0)
+        st.flag = (st.flag + senders) & MASK32
+        reached = ((st.flag - st.counter) & MASK32) >= 2 * W
+        if not reached.all():
+            _set_err(st, ETIMEOUT)
+        st.counter = np.where(reached, (st.counter + 2 * W) & MASK32, st.counter)
+
+    # 5. rank-order reduce of the staged slots.
+    out = _reduce([st.slots[par][r] for r in range(W)])
+
+    # 6. exit: zero-resetting pad barrier (Pattern 2), epoch flip, last block out.
+    _pad_barrier(st)
     st.epoch = (st.epoch + 1) % 2
     st.blocks[1] = 0
     st.seq = seq

@@ -13,6 +13,10 @@
 * Failure detection without any GPU fault: a missing end-barrier signal
   makes the bounded waits expire (ARX_ETIMEOUT read by the host, context
   usable after a reset); a corrupted epoch reports ARX_ESTATE.
+* All of the above in each barrier variant (``ARX_SYNC_SEMAPHORE``,
+  ``ARX_SYNC_PAD``, ``ARX_SYNC_PAD_FENCED``: common.cuh's Semaphore barriers,
+  or triton_barrier.py's pad barrier in its Patterns 0/1/2, relaxed or
+  acq_rel), and switching variants between steps of one context.
 """
 
 from concurrent.futures import ThreadPoolExecutor
@@ -29,6 +33,7 @@ from test_gpu_reduce import assert_bits_equal
 pytestmark = pytest.mark.gpu
 
 M32 = 0xFFFFFFFF
+SYNCS = ["semaphore", "pad", "pad_fenced"]
 
 
 @pytest.fixture(scope="module")
@@ -40,12 +45,17 @@ def dev(arx):
 class Ctx:
     """A context plus typed views of its workspace words."""
 
-    def __init__(self, arx, dev, W, max_n, nblocks=0):
+    def __init__(self, arx, dev, W, max_n, nblocks=0, sync="semaphore"):
         self.arx = arx
         nbytes = arx.arx_ctx_workspace_bytes(W, max_n, nblocks)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self.ctx = arx.arx_ctx_init(self.ws, W, max_n, nblocks)
         self.W, self.B = W, self.ctx.nblocks
+        self.set_sync(sync)
+
+    def set_sync(self, sync):
+        self.arx.arx_ctx_set_sync(self.ctx, SYNCS.index(sync))
+        self.sync = sync
 
     def words(self):
         c, W, B = self.ctx, self.W, self.B
@@ -93,10 +103,11 @@ def _step(arx, c: Ctx, x: torch.Tensor, dev, out_offset=0, in_offset=0):
     return out
 
 
+@pytest.mark.parametrize("sync", SYNCS)
 @pytest.mark.parametrize("W", range(1, 9))
-def test_single_step_every_w(arx, dev, W):
+def test_single_step_every_w(arx, dev, W, sync):
     for n, nblocks in ((131072, 0), (1000003, 0), (13, 1), (4096 + 5, 3)):
-        c = Ctx(arx, dev, W, n, nblocks)
+        c = Ctx(arx, dev, W, n, nblocks, sync)
         x = sp.partials(W, n, "special" if n < 5000 else "normal", seed=W * 7 + n)
         out = _step(arx, c, x, dev)
         st, seq, err = arx.arx_ctx_query(c.ctx)
@@ -140,9 +151,10 @@ def test_step_output_aliases_an_input(arx, dev):
                       oracle.reduce(list(sp.to_u16_numpy(x))), "step in place")
 
 
+@pytest.mark.parametrize("sync", SYNCS)
 @pytest.mark.parametrize("W,n,B,k", [(8, 131072, 0, 5), (3, 777, 2, 4), (5, 65536 + 7, 7, 3), (1, 100, 1, 2)])
-def test_protocol_words_follow_the_model(arx, dev, W, n, B, k):
-    c = Ctx(arx, dev, W, n, B)
+def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync):
+    c = Ctx(arx, dev, W, n, B, sync)
     st = model.State(W=W, B=c.B)
     hist = []
     for s in range(k):
@@ -150,11 +162,11 @@ def test_protocol_words_follow_the_model(arx, dev, W, n, B, k):
         u = list(sp.to_u16_numpy(x))
         hist.append(u)
         out = _step(arx, c, x, dev)
-        want = model.step(st, u)
+        want = model.step(st, u, sync=sync)
         assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s}")
         _compare_to_model(c.words(), st)
-    assert (c.words()["flag"] == 2 * W * k).all()
+    assert (c.words()["flag"] == (2 * W * k if sync == "semaphore" else 0)).all()
     for r in range(W):
         assert np.array_equal(c.slot(k & 1, r, n), hist[k - 1][r])
         if k >= 2:
@@ -187,9 +199,10 @@ def test_unsigned_wrap_of_seq_and_flags(arx, dev):
     assert w["seq"] == 1
 
 
-def test_timeout_is_reported_and_context_recovers(arx, dev):
+@pytest.mark.parametrize("sync", SYNCS)
+def test_timeout_is_reported_and_context_recovers(arx, dev, sync):
     W, n = 4, 8192
-    c = Ctx(arx, dev, W, n, 2)
+    c = Ctx(arx, dev, W, n, 2, sync)
     x = sp.partials(W, n, "normal", seed=8)
     _step(arx, c, x, dev)
     assert arx.arx_ctx_query(c.ctx)[:2] == (arx.ARX_OK, 1)
@@ -198,10 +211,13 @@ def test_timeout_is_reported_and_context_recovers(arx, dev):
     _step(arx, c, x, dev)
     st, seq, err = arx.arx_ctx_query(c.ctx)
     assert st == arx.ARX_ETIMEOUT
-    assert err & 0xFF == arx.ARX_ETIMEOUT and (err >> 8) & 15 == 2  # stage: end-barrier wait
+    # stage: the end-barrier wait (2 on the Semaphores, 9 on the pad)
+    assert err & 0xFF == arx.ARX_ETIMEOUT and (err >> 8) & 15 == (2 if sync == "semaphore" else 9)
     assert seq == 2                                  # the kernel still finished
     w = c.words()
-    assert not w["pad"].any() and w["blocks"] == [0, 0]
+    assert w["blocks"] == [0, 0]
+    if sync == "semaphore":
+        assert not w["pad"].any()
     # Recovery: zero the protocol words, clear the fault, step again.
     arx.arx_ctx_set_fault(c.ctx, -1)
     arx.arx_ctx_reset(c.ctx)
@@ -223,24 +239,46 @@ def test_epoch_mismatch_reports_state_error(arx, dev):
     assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))), "data")
 
 
+def test_switching_sync_modes_between_steps(arx, dev):
+    W, n = 6, 30011
+    c = Ctx(arx, dev, W, n, 3)
+    st = model.State(W=W, B=c.B)
+    for s, sync in enumerate(["semaphore", "pad", "pad_fenced", "semaphore", "pad_fenced", "pad", "semaphore"]):
+        c.set_sync(sync)
+        x = sp.partials(W, n, "normal", seed=300 + s)
+        out = _step(arx, c, x, dev)
+        want = model.step(st, list(sp.to_u16_numpy(x)), sync=sync)
+        assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK, sync
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s} ({sync})")
+        _compare_to_model(c.words(), st)
+
+
+def test_unknown_sync_mode_is_rejected(arx, dev):
+    c = Ctx(arx, dev, 2, 64, 1)
+    with pytest.raises(arx.ArxError):
+        arx.arx_ctx_set_sync(c.ctx, 3)
+    assert c.ctx.sync_mode == arx.ARX_SYNC_SEMAPHORE
+
+
 # ---- 10,000 steps in one CUDA graph --------------------------------------------------------
 
 GRAPH_STEPS = sp.GRAPH_STEPS
 W8, N8 = 8, sp.N_32x4096
 
 
-def test_ten_thousand_steps_in_one_graph(arx, dev):
+@pytest.fixture(scope="module")
+def graph_workload(dev):
+    """10,000 steps of fresh normal(0, 1) partials (seed 4 + step) on the device, with
+    the oracle's output of every step and the last two steps' inputs."""
     steps, chunk = GRAPH_STEPS, 500
-    c = Ctx(arx, dev, W8, N8)
     inputs = torch.empty(steps, W8, N8, dtype=torch.bfloat16, device=dev)
-    outputs = torch.zeros(steps, N8, dtype=torch.bfloat16, device=dev)
     want = np.empty((steps, N8), dtype=np.uint16)
     last_two = {}
     host = torch.empty(chunk, W8, N8, dtype=torch.int16).pin_memory()
     host_np = host.numpy().view(np.uint16)
 
-    # Step s draws fresh normal(0, 1) partials from seed 4 + s.  Torch's RNG and
-    # the oracle's C code release the GIL, so threads generate in parallel.
+    # Torch's RNG and the oracle's C code release the GIL, so threads generate
+    # in parallel.
     def fill(s, base):
         u = sp.to_u16_numpy(sp.graph_step_partials(s))
         host_np[s - base] = u
@@ -254,7 +292,17 @@ def test_ten_thousand_steps_in_one_graph(arx, dev):
             list(ex.map(lambda s: fill(s, base), range(base, hi)))
             inputs[base:hi].view(torch.int16).copy_(host[: hi - base])
     torch.cuda.synchronize()
+    yield inputs, want, last_two
+    del inputs
+    torch.cuda.empty_cache()
 
+
+@pytest.mark.parametrize("sync", SYNCS)
+def test_ten_thousand_steps_in_one_graph(arx, dev, graph_workload, sync):
+    inputs, want, last_two = graph_workload
+    steps = inputs.shape[0]
+    c = Ctx(arx, dev, W8, N8, 0, sync)
+    outputs = torch.zeros(steps, N8, dtype=torch.bfloat16, device=dev)
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
@@ -269,7 +317,8 @@ def test_ten_thousand_steps_in_one_graph(arx, dev):
     assert bad.size == 0, f"{bad.size} of {steps} steps differ; first step {int(bad[0])}"
     w = c.words()
     assert not w["pad"].any(), "signal pad must be all zero after the last step"
-    assert (w["flag"] == 2 * W8 * steps).all() and (w["counter"] == w["flag"]).all()
+    flags = 2 * W8 * steps if sync == "semaphore" else 0   # the pad variants leave the Semaphores alone
+    assert (w["flag"] == flags).all() and (w["counter"] == w["flag"]).all()
     assert (w["epoch"] == steps % 2).all() and w["blocks"] == [0, 0]
     assert w["published"] == steps
     for r in range(W8):

@@ -89,3 +89,46 @@ def test_parity_alternates_banks():
     assert np.array_equal(st.slots[1][0], a[0]) and np.array_equal(st.slots[0][0], b[0])
     P.step(st, c)          # seq 3 -> bank 1 again, bank 0 untouched
     assert np.array_equal(st.slots[1][1], c[1]) and np.array_equal(st.slots[0][1], b[1])
+
+
+# ---- barrier variants (triton_barrier.py Patterns 0/1/2 on the signal pad) ----------------
+
+@pytest.mark.parametrize("sync", ["pad", "pad_fenced"])
+@pytest.mark.parametrize("W,B,k", [(1, 1, 1), (3, 2, 4), (8, 3, 5)])
+def test_pad_modes_closed_form(sync, W, B, k):
+    st = P.State(W=W, B=B)
+    for s in range(k):
+        x = _inputs(W, 32, s)
+        assert np.array_equal(P.step(st, x, sync=sync), oracle.reduce(x))
+    # Three pad barriers per step, each pairing every send with one wait, so
+    # the pad is zero after every step; the Semaphores are never touched.
+    assert not st.pad.any()
+    assert not st.flag.any() and not st.counter.any()
+    assert (st.epoch == k % 2).all() and st.blocks == [0, 0]
+    assert st.seq == k and st.published == k and st.err == 0
+
+
+def test_switching_modes_between_steps():
+    W, B = 4, 2
+    st = P.State(W=W, B=B)
+    modes = ["semaphore", "pad", "pad_fenced", "semaphore", "pad", "semaphore"]
+    for s, m in enumerate(modes):
+        P.step(st, _inputs(W, 16, s), sync=m)
+    # Only the Semaphore steps move the flags, by 2W each.
+    assert st.err == 0
+    assert (st.flag == 2 * W * modes.count("semaphore")).all() and (st.counter == st.flag).all()
+    assert not st.pad.any() and (st.epoch == len(modes) % 2).all()
+
+
+@pytest.mark.parametrize("sync", ["pad", "pad_fenced"])
+def test_pad_mode_missing_end_signal_reports_timeout(sync):
+    st = P.State(W=3, B=2)
+    P.step(st, _inputs(3, 16, 0), sync=sync)
+    assert st.err == 0
+    P.step(st, _inputs(3, 16, 1), skip_end_signal_rank=1, sync=sync)
+    assert st.err == P.ETIMEOUT
+
+
+def test_unknown_mode_is_rejected():
+    with pytest.raises(ValueError):
+        P.step(P.State(W=1, B=1), _inputs(1, 8, 0), sync="fenced")
