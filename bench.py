@@ -18,12 +18,15 @@ Timing rules followed:
 * nvidia-smi clocks and throttle reasons are sampled around the timed region.
 
 Extra objects on the one JSON line: ``roofline`` (the reduce kernel against
-the measured HBM copy bandwidth), ``cpu_baseline`` (the CPU oracle on the
-host's cores, a bounded sample), ``e2e`` (the same metric through
-``arx_reduce_host`` with pinned host buffers, copies included),
-``bandwidth`` (bandwidth-bound sizes: W=4 [1024, 8192] in place, W=8 at
-16 MiB and 256 MiB per partial), ``protocol`` (``arx_step`` per step in a
-captured graph).
+the measured HBM copy bandwidth), ``cpu_baseline`` / ``cpu_baseline_1thread``
+(the CPU oracle on all host cores and on one, bounded samples), ``e2e`` (the
+same metric through ``arx_reduce_host`` with pinned host buffers, the
+partials crossing the CPU-GPU link every call, against the link's measured
+pinned copy rate), ``bandwidth`` (bandwidth-bound sizes: W=4 [1024, 8192] in
+place, W=8 at 16 MiB and 256 MiB per partial), ``protocol`` (``arx_step``
+per step in a captured graph, for each barrier variant), ``latency_floor``
+(the same call with 1 KiB partials), ``hot_l2`` (inputs left in L2,
+labelled), ``stream_launch`` (eager launches through the binding, no graph).
 
 ``--impl reference`` times the CPU oracle instead (the reference arm: there
 is no reference implementation to install, the pages hold no code to build).
@@ -360,9 +363,13 @@ def run_native(args) -> None:
     extra = {}
     if not args.quick:
         extra["latency_floor"] = floor_point(torch, arx, dev, stream, l2, W, n, per_call)
+        extra["hot_l2"] = hot_l2_point(torch, arx, stream, slot_lists, outs, W, n)
+        extra["stream_launch"] = stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R)
         extra["bandwidth"] = bandwidth_points(torch, arx, sp, dev, stream, l2)
         extra["protocol"] = protocol_point(torch, arx, sp, dev, stream, l2, args.workload)
-        extra["e2e"] = e2e_point(torch, arx, sp, dev, stream, args.workload, max(200, min(args.steps, 5000)), l2)
+        link = pinned_copy_gbs(torch, dev)
+        extra["e2e"] = e2e_point(torch, arx, sp, dev, stream, args.workload, max(200, min(args.steps, 5000)),
+                                 l2, link)
     if rank != 0:
         return
     peaks = measured_peaks()
@@ -371,7 +378,7 @@ def run_native(args) -> None:
     peak = float(peak) if peak else FALLBACK_HBM_GBS
     achieved = gbs(bytes_call, per_call)
     traffic = stored_traffic(args.workload)
-    cpu = None
+    cpu = cpu1 = None
     if not args.no_cpu_baseline:
         import oracle
         threads = oracle.default_threads()
@@ -379,6 +386,9 @@ def run_native(args) -> None:
         cpu = {"value": r["gbs"], "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{r['calls']} full calls of the {args.workload} workload "
                          f"(W={W}, n={n}) in {r['seconds']:.1f} s on {threads} host threads"}
+        r1 = time_oracle(W, n, None, args.cpu_seconds / 2, 1, spec["seed"], spec["dist"])
+        cpu1 = {"value": r1["gbs"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{r1['calls']} full calls in {r1['seconds']:.1f} s on 1 host thread"}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
@@ -391,13 +401,29 @@ def run_native(args) -> None:
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic,
-                     "kernel": f"reduce_vec_kernel<{W}>", "algorithmic_bytes_per_launch": bytes_call},
+                     "kernel": reduce_kernel_name(W, n, alias), "algorithmic_bytes_per_launch": bytes_call},
         "cpu_baseline": cpu,
+        "cpu_baseline_1thread": cpu1,
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
     line.update(extra)
     print(json.dumps(line), flush=True)
+
+
+HALF_MAX_ELEMS = 1 << 22   # the library's switch from 8-byte to 16-byte vectors
+
+
+def reduce_kernel_name(W: int, n: int, alias: bool) -> str:
+    """The kernel the library launches for this shape (its launch policy, restated)."""
+    a = "true" if alias else "false"
+    if n <= HALF_MAX_ELEMS:
+        return f"reduce_half_kernel<{W}, 256, {a}>"
+    if W <= 2:
+        return f"reduce_vec_kernel<{W}, 128, 2, pipelined, {a}>"
+    if W <= 4:
+        return f"reduce_vec_kernel<{W}, 256, 1, pipelined, {a}>"
+    return f"reduce_vec_kernel<{W}, 256, 2, {a}>"
 
 
 def bandwidth_points(torch, arx, sp, dev, stream, l2) -> list:
@@ -456,30 +482,111 @@ def floor_point(torch, arx, dev, stream, l2, W, n, per_call) -> dict:
             "marginal_GBs": gbs((W + 1) * n * 2, above) if above > 0 else None}
 
 
+SYNC_MODES = ("semaphore", "pad", "pad_fenced")
+
+
 def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:
-    """arx_step per step (W=8, [32,4096]) in captured graphs, fresh input sets rotating."""
+    """arx_step per step (W=8, [32,4096]) in captured graphs, fresh input sets rotating,
+    for each barrier variant (Semaphore barriers; pad barrier Patterns 0/1/2; all acq_rel)."""
     W, n = 8, sp.N_32x4096
     x, _ = sp.workload(workload)
     R = rotation_sets(W * n * 2 * 2, l2)
     parts = torch.empty(R, W, n, dtype=torch.bfloat16, device=dev)
     parts.copy_(x.to(dev).unsqueeze(0).expand(R, W, n))
     outs = torch.empty(R, n, dtype=torch.bfloat16, device=dev)
-    ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
-    ctx = arx.arx_ctx_init(ws, W, n)
     lists = [[parts[k, r] for r in range(W)] for k in range(R)]
-
-    def call(i):
-        arx.arx_step(ctx, lists[i % R], outs[i % R], stream=stream)
-
     steps = 2000
-    t = timed_graph_calls(torch, stream, call, steps, 10)
-    st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
-    return {"W": W, "n": n, "blocks_per_rank": ctx.nblocks, "steps": steps,
-            "us_per_step": t / steps * 1e6, "status": arx.arx_status_string(st), "seq": seq,
-            "reduce_model_GBs": gbs((W + 1) * n * 2, t / steps)}
+    res = {"W": W, "n": n, "steps": steps, "modes": {}}
+    for mode_index, mode in enumerate(SYNC_MODES):
+        ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
+        ctx = arx.arx_ctx_init(ws, W, n)
+        arx.arx_ctx_set_sync(ctx, mode_index)
+
+        def call(i, ctx=ctx):
+            arx.arx_step(ctx, lists[i % R], outs[i % R], stream=stream)
+
+        t = timed_graph_calls(torch, stream, call, steps, 10)
+        st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
+        res["blocks_per_rank"] = ctx.nblocks
+        res["modes"][mode] = {"us_per_step": t / steps * 1e6, "status": arx.arx_status_string(st),
+                              "seq": seq, "reduce_model_GBs": gbs((W + 1) * n * 2, t / steps)}
+    res["us_per_step"] = res["modes"]["semaphore"]["us_per_step"]
+    return res
 
 
-def e2e_point(torch, arx, sp, dev, stream, workload, steps, l2) -> dict:
+def pinned_copy_gbs(torch, dev, nbytes: int = 1 << 26, reps: int = 5) -> dict:
+    """Best-of-reps copy-engine bandwidth between pinned host memory and the device
+    (the CPU-GPU link's measured rate, the denominator of the host-buffer path)."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name in ("h2d", "d2h"):
+        best = float("inf")
+        for _ in range(reps):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            if name == "h2d":
+                d.copy_(h, non_blocking=True)
+            else:
+                h.copy_(d, non_blocking=True)
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e) / 1e3)
+        out[name] = nbytes / best / 1e9
+    out["bytes"] = nbytes
+    return out
+
+
+def stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R) -> dict:
+    """The headline call launched eagerly through the Python binding (no graph).
+
+    back_to_back: K calls enqueued in a row, events around the batch (bound by the
+    host's launch rate); single_call: events around one call at a time, GPU idle
+    before each, median over the calls (includes the launch latency).
+    """
+    def call(i):
+        arx.arx_reduce(slot_lists[i % R], outs[i % R], stream=stream)
+
+    K = 2000
+    with torch.cuda.stream(stream):
+        for i in range(50):
+            call(i)
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for i in range(K):
+            call(i)
+        e.record(stream)
+        torch.cuda.synchronize()
+        b2b = s.elapsed_time(e) / 1e3 / K
+        single = []
+        for i in range(1000):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            call(i)
+            e.record(stream)
+            e.synchronize()
+            single.append(s.elapsed_time(e) / 1e3)
+    return {"back_to_back_us_per_call": b2b * 1e6, "calls": K,
+            "single_call_us_median": statistics.median(single) * 1e6, "single_calls": len(single)}
+
+
+def hot_l2_point(torch, arx, stream, slot_lists, outs, W, n) -> dict:
+    """HOT-L2 figure, labelled as such: the same buffer set every call, so the
+    inputs are served from L2 (not the headline, which rotates beyond L2)."""
+    def call(i):
+        arx.arx_reduce(slot_lists[0], outs[0], stream=stream)
+
+    calls = 20000
+    t = timed_graph_calls(torch, stream, call, calls, 100)
+    return {"label": "hot L2 (one buffer set reused)", "us_per_call": t / calls * 1e6,
+            "GBs": gbs((W + 1) * n * 2, t / calls)}
+
+
+def e2e_point(torch, arx, sp, dev, stream, workload, steps, l2, link) -> dict:
     """The metric through arx_reduce_host: pinned host partials in, host result out, per step.
 
     The host sets rotate like the device ones (footprint above 3x L2): the GPU
@@ -501,9 +608,17 @@ def e2e_point(torch, arx, sp, dev, stream, workload, steps, l2) -> dict:
     import oracle
     want = oracle.reduce(list(sp.to_u16_numpy(x)))
     ok = bool((sp.to_u16_numpy(hout[(steps - 1) % R]) == want).all())
-    return {"value": gbs((W + 1) * n * 2, t / steps), "unit": "GB/s",
+    value = gbs((W + 1) * n * 2, t / steps)
+    # Link roofline: the bytes cross the CPU-GPU link once each way (W partials
+    # in, the sum out); the denominator is the measured pinned copy rate.
+    peak = link["h2d"]
+    return {"value": value, "unit": "GB/s",
             "us_per_call": t / steps * 1e6, "steps": steps,
             "h2d_bytes_per_step": W * n * 2, "d2h_bytes_per_step": n * 2, "bit_exact": ok,
+            "roofline": {"bound": "c2c", "achieved": value, "peak": peak, "unit": "GB/s",
+                         "frac": value / peak,
+                         "peak_source": f"measured in this run: pinned host->device copy of "
+                                        f"{link['bytes'] >> 20} MiB (device->host {link['d2h']:.0f} GB/s)"},
             "path": "arx_reduce_host on page-locked host buffers: the kernel reads the partials "
                     "and writes the sum in host memory over NVLink-C2C (no staging copies); "
                     f"{R} rotating host sets"}

@@ -9,12 +9,17 @@
 // GB300 design (the pages' fixed grid of at most 8 blocks and 512 KB cap are
 // dropped):
 //  * persistent grid-stride loop, grid = SMs x resident blocks (capped by the
-//    work), coalesced 512-byte warp accesses per slot, L1 bypassed;
-//  * U independent groups per thread per iteration, all W*U loads issued
-//    before the first add (Little's law against HBM3e latency);
+//    work), coalesced warp accesses per slot, L1 bypassed;
+//  * up to 2^22 elements per partial (latency-bound and medium messages):
+//    8-byte vectors (4 elements) per slot, one per thread per iteration --
+//    twice the threads of the 16-byte form at half the registers each, so
+//    more loads are in flight per SM and the message spreads over more SMs;
+//  * above (bandwidth-bound): 16-byte vectors, U independent groups per
+//    thread per iteration, all W*U loads issued before the first add
+//    (Little's law against HBM3e latency);
 //  * software pipelining (kPipe): the next iteration's loads are in flight
 //    while the current groups are summed and stored -- measured best for
-//    small and medium messages and for W <= 4;
+//    W <= 4 at large sizes;
 //  * programmatic dependent launch: the kernel waits on its stream
 //    predecessor (griddepcontrol.wait) before touching memory and lets its
 //    successor start launching at once, which hides most of the launch gap
@@ -27,12 +32,19 @@
 namespace arx {
 namespace {
 
+// Kernel arguments.  The 16-byte-aligned body's pointers are computed on the
+// host (element `head` of each slot and of out), so the streaming loop does no
+// address arithmetic on them: a form that offset the slot pointers in the
+// kernel and also used them for the scalar edges after the loop took 46
+// instead of 30 registers at W = 8 and ran 30 % slower.
 struct VecArgs {
-  const uint16_t* slot[kMaxW];  // element 0 of each slot
+  const uint16_t* body_src[kMaxW];  // element `head` of each slot (16-byte aligned)
+  uint16_t* body_dst;               // element `head` of out
+  size_t groups;                    // 16-byte groups in the body
+  const uint16_t* slot[kMaxW];      // element 0 of each slot (scalar edges)
   uint16_t* out;
   size_t n;        // elements
   size_t head;     // scalar elements before the first 16-byte boundary
-  size_t groups;   // 16-byte groups after the head
 };
 
 template <int W>
@@ -43,12 +55,24 @@ __device__ __forceinline__ void scalar_element(const VecArgs& a, size_t e) {
   a.out[e] = round_bf16(acc);
 }
 
-template <bool kAlias>
-__device__ __forceinline__ uint4 load_group(const uint4* p) {
+template <bool kAlias, typename V>
+__device__ __forceinline__ V load_group(const V* p) {
   if constexpr (kAlias) {
     return ld_stream(p);
   } else {
     return ld_stream_nc(p);
+  }
+}
+
+// Scalar head (before the first 16-byte boundary) and tail (after the last
+// full 16-byte group): at most 7 + 7 elements, done by the last block.
+template <int W>
+__device__ __forceinline__ void head_and_tail(const VecArgs& a) {
+  const size_t tail = a.n - a.head - 8 * a.groups;
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x < a.head + tail) {
+    const size_t t = threadIdx.x;
+    const size_t e = t < a.head ? t : a.head + 8 * a.groups + (t - a.head);
+    scalar_element<W>(a, e);
   }
 }
 
@@ -80,8 +104,8 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
   dependent_launch_prologue();
   const uint4* src[W];
 #pragma unroll
-  for (int r = 0; r < W; ++r) src[r] = reinterpret_cast<const uint4*>(a.slot[r] + a.head);
-  uint4* dst = reinterpret_cast<uint4*>(a.out + a.head);
+  for (int r = 0; r < W; ++r) src[r] = reinterpret_cast<const uint4*>(a.body_src[r]);
+  uint4* dst = reinterpret_cast<uint4*>(a.body_dst);
 
   const size_t stride = size_t(gridDim.x) * T;
   const size_t step = size_t(U) * stride;
@@ -123,14 +147,27 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
     st_global(dst + g, sum_vectors<W>(v));
   }
 
-  // Scalar head (before the first 16-byte boundary) and tail (after the last
-  // full group): at most 7 + 7 elements, done by the last block.
-  const size_t tail = a.n - a.head - 8 * G;
-  if (blockIdx.x == gridDim.x - 1 && threadIdx.x < a.head + tail) {
-    const size_t t = threadIdx.x;
-    const size_t e = t < a.head ? t : a.head + 8 * G + (t - a.head);
-    scalar_element<W>(a, e);
+  head_and_tail<W>(a);
+}
+
+// 8-byte form: the 16-byte-aligned body as 2 * groups vectors of 4 elements,
+// one vector per slot per thread per iteration.
+template <int W, int T, bool kAlias>
+__global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
+  dependent_launch_prologue();
+  const uint2* src[W];
+#pragma unroll
+  for (int r = 0; r < W; ++r) src[r] = reinterpret_cast<const uint2*>(a.body_src[r]);
+  uint2* dst = reinterpret_cast<uint2*>(a.body_dst);
+  const size_t H = 2 * a.groups;
+  const size_t stride = size_t(gridDim.x) * T;
+  for (size_t h = size_t(blockIdx.x) * T + threadIdx.x; h < H; h += stride) {
+    uint2 v[W];
+#pragma unroll
+    for (int r = 0; r < W; ++r) v[r] = load_group<kAlias>(src[r] + h);
+    st_global(dst + h, sum_halves<W>(v));
   }
+  head_and_tail<W>(a);
 }
 
 // Pointers with different addresses mod 16: one element per thread per step.
@@ -186,21 +223,36 @@ cudaError_t launch_vec(const VecArgs& a, int dev, int sms, cudaStream_t stream) 
   return launch_dependent(k, blocks, T, stream, a);
 }
 
-// Measured policy (bench.py --sweep and the shape sweep on GB300):
-//  W <= 2: 128 threads, U = 2, pipelined, at every size;
-//  W 3-4:  256 threads, U = 1, pipelined;
-//  W >= 5: 256 threads, U = 1, pipelined up to 2 MiB per partial; above,
-//          U = 2 without pipelining (more loads in flight per thread).
-constexpr size_t kLargePartialElems = size_t(1) << 20;
+template <int W, int T, bool kAlias>
+cudaError_t launch_half(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
+  static int cache[kMaxDevices];
+  cudaError_t err = cudaSuccess;
+  auto k = reduce_half_kernel<W, T, kAlias>;
+  const int per_sm = blocks_per_sm(k, T, dev, cache, &err);
+  if (per_sm < 1) return err;
+  size_t blocks = (2 * a.groups + T - 1) / T;
+  const size_t cap = size_t(sms) * size_t(per_sm);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_dependent(k, blocks, T, stream, a);
+}
+
+// Measured policy (launch-shape sweeps of W = 2, 4, 8 from 2^15 to 2^27
+// elements per partial on GB300, CUDA-graph replays, inputs beyond L2):
+//  n <= 2^22: 8-byte vectors, 256 threads, every W;
+//  above:     16-byte groups -- W <= 2: 128 threads, U = 2, pipelined;
+//             W 3-4: 256 threads, U = 1, pipelined; W >= 5: 256 threads,
+//             U = 2 without pipelining (more loads in flight per thread).
+constexpr size_t kHalfMaxElems = size_t(1) << 22;
 
 template <int W, bool kAlias>
 cudaError_t launch_policy(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
+  if (a.n <= kHalfMaxElems) return launch_half<W, 256, kAlias>(a, dev, sms, stream);
   if constexpr (W <= 2) {
     return launch_vec<W, 128, 2, true, kAlias>(a, dev, sms, stream);
   } else if constexpr (W <= 4) {
     return launch_vec<W, 256, 1, true, kAlias>(a, dev, sms, stream);
   } else {
-    if (a.n <= kLargePartialElems) return launch_vec<W, 256, 1, true, kAlias>(a, dev, sms, stream);
     return launch_vec<W, 256, 2, false, kAlias>(a, dev, sms, stream);
   }
 }
@@ -228,6 +280,8 @@ cudaError_t launch_w(const ReduceCall& c, cudaStream_t stream) {
     if (head > c.n) head = c.n;
     a.head = head;
     a.groups = (c.n - head) / 8u;
+    for (int r = 0; r < W; ++r) a.body_src[r] = c.slot[r] + head;
+    a.body_dst = c.out + head;
     err = c.out_aliases_slot ? launch_policy<W, true>(a, dev, sms, stream)
                              : launch_policy<W, false>(a, dev, sms, stream);
     if (err != cudaSuccess) return err;

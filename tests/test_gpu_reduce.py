@@ -113,6 +113,23 @@ def test_in_place_small_and_ragged(arx, dev, W):
         assert_bits_equal(_run(arx, dev, x, alias=True), want, f"alias W={W} n={n}")
 
 
+@pytest.mark.parametrize("W", [1, 3, 8])
+@pytest.mark.parametrize("n", [(1 << 22) - 3, (1 << 22) + 9])
+def test_both_vector_forms_ragged_misaligned_in_place(arx, dev, W, n):
+    # Sizes just below and above the switch from 8-byte to 16-byte vectors,
+    # with a scalar head (every pointer 2 bytes past a 16-byte boundary), a
+    # ragged tail, and the output aliasing the last slot.
+    x = sp.partials(W, n, "normal", seed=n % 1000 + W)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+    buf = torch.zeros(W, n + 16, dtype=torch.bfloat16, device=dev)
+    buf[:, 1:1 + n] = x.to(dev)
+    slots = [buf[r, 1:1 + n] for r in range(W)]
+    arx.arx_reduce(slots, slots[W - 1])
+    torch.cuda.synchronize()
+    assert_bits_equal(slots[W - 1].cpu().view(torch.int16).numpy(), want, f"W={W} n={n} in place")
+    assert not buf[W - 1, 0].view(torch.int16).item() and not buf[W - 1, 1 + n:].view(torch.int16).any()
+
+
 def test_alias_to_last_slot(arx, dev):
     x = sp.partials(5, 40000, "normal", seed=9)
     want = oracle.reduce(list(sp.to_u16_numpy(x)))
