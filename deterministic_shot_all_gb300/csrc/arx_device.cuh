@@ -142,6 +142,16 @@ __device__ __forceinline__ void st_global(uint2* p, const uint2& v) {
   asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+
+// Wait for the previous kernel of the stream (when launched as its
+// programmatic dependent) before any global access, then allow the next one
+// to begin launching; it waits in the same way before touching memory.
+__device__ __forceinline__ void dependent_launch_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // ---- scoped atomics and loads for the protocol words (one GPU: .gpu scope) -------
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {

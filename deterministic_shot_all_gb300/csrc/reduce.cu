@@ -76,14 +76,6 @@ __device__ __forceinline__ void head_and_tail(const VecArgs& a) {
   }
 }
 
-// Wait for the previous kernel of the stream (when launched as its
-// programmatic dependent) before any global access, then allow the next one
-// to begin launching; it waits in the same way before touching memory.
-__device__ __forceinline__ void dependent_launch_prologue() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" :::);
-}
-
 template <int W, int U, bool kAlias>
 __device__ __forceinline__ void load_batch(uint4 (&v)[U][W], const uint4* const (&src)[W], size_t g,
                                            size_t stride) {

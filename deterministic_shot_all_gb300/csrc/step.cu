@@ -42,6 +42,17 @@
 // cap): on expiry the block records ARX_ETIMEOUT with its stage, rank and
 // block in the error word and carries on, so the kernel always finishes and
 // the host reads the status.  The pages' waits are unbounded; these are not.
+//
+// Latency choices (measured on GB300, W = 8, bf16 [32, 4096]): the kernel is
+// a programmatic dependent of the previous kernel on its stream (it waits for
+// it before touching memory, and lets the next one launch at once); fenced
+// waits poll with relaxed loads and fence once after success (the
+// fence-after-read form of acquire); the exit writes the flipped epoch from
+// the value read at entry and counts blocks out without fences -- seq,
+// epochs and counters are read only by later kernels on the stream (ordered
+// by the kernel boundary) and by the host after a synchronisation, never by
+// another block of the same launch.  The pages fence there because a host
+// proxy and remote GPUs observe those words while the kernel runs.
 #include "arx_device.cuh"
 #include "arx_internal.h"
 
@@ -96,16 +107,21 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code, uint3
   atomicCAS(err, 0u, word);
 }
 
-// Wait until flag - base >= target (unsigned), bounded.  kFence selects an
-// acquire load (end stage) or a relaxed one (start stage).
+// Wait until flag - base >= target (unsigned), bounded.  Polls with relaxed
+// loads; kFence (end stage) adds a fence after the successful poll, which
+// makes it an acquire of everything released before the flag reached the
+// target (the start stage is unfenced).
 template <bool kFence>
 __device__ bool semaphore_wait(const uint32_t* flag, uint32_t base, uint32_t target,
                                uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
   const uint64_t cap = spin_cap(timeout_ns);
   for (uint64_t spins = 0;; ++spins) {
-    const uint32_t v = kFence ? ld_acquire_gpu(flag) : ld_relaxed_gpu(flag);
-    if (v - base >= target) return true;
+    const uint32_t v = ld_relaxed_gpu(flag);
+    if (v - base >= target) {
+      if constexpr (kFence) __threadfence();
+      return true;
+    }
     if ((spins & 15u) == 15u) {
       if (global_timer_ns() - t0 > timeout_ns || spins > cap) return false;
       backoff(spins);
@@ -193,12 +209,16 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   const uint32_t total_blocks = B * uint32_t(W);
 
   __shared__ uint32_t s_seq;
+  dependent_launch_prologue();
 
-  // 1. seq / parity; epoch check.
+  // 1. seq / parity; epoch check (both words loaded back to back).
+  uint32_t epoch_in = 0;  // thread 0 only
   if (tid == 0) {
-    const uint32_t seq = ld_relaxed_gpu(&hdr->seq) + 1u;
+    const uint32_t done = ld_relaxed_gpu(&hdr->seq);
+    epoch_in = epoch[r * B + b];
+    const uint32_t seq = done + 1u;
     s_seq = seq;
-    if (epoch[r * B + b] != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
+    if (epoch_in != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
 
   // 2. start barrier.
@@ -278,7 +298,6 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     }
     if (warp == r) {
       if (semaphore_wait<true>(&own.flag, base, 2u * uint32_t(W), a.timeout_ns)) {
-        __threadfence();
         own.counter = base + 2u * uint32_t(W);
       } else {
         record_error(&hdr->err, kErrTimeout, kEndWait, r, b);
@@ -338,11 +357,9 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
                             kPadWait);
   __syncthreads();
   if (tid == 0) {
-    epoch[r * B + b] = (epoch[r * B + b] + 1u) % 2u;  // PushController::exit
-    __threadfence();
+    epoch[r * B + b] = (epoch_in + 1u) % 2u;  // PushController::exit
     if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
       hdr->blocks[1] = 0u;
-      __threadfence();
       st_relaxed_gpu(&hdr->seq, seq);
     }
   }
@@ -395,12 +412,15 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   // Every block of the grid waits on others: the launch must make them all
-  // resident at once.
-  cudaLaunchAttribute attr[1];
+  // resident at once.  It is also a programmatic dependent of the previous
+  // kernel on the stream (see dependent_launch_prologue).
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t err = cudaErrorInvalidValue;
   switch (c.sync_mode) {
     case kSyncSemaphore: err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore>, a); break;
