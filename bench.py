@@ -24,7 +24,8 @@ same metric through ``arx_reduce_host`` with pinned host buffers, the
 partials crossing the CPU-GPU link every call, against the link's measured
 pinned copy rate), ``bandwidth`` (bandwidth-bound sizes: W=4 [1024, 8192] in
 place, W=8 at 16 MiB and 256 MiB per partial), ``protocol`` (``arx_step``
-per step in a captured graph, for each barrier variant), ``latency_floor``
+per step in a captured graph, for each barrier variant), ``protocol_host_slots``
+(the step with its slot banks in page-locked host memory), ``latency_floor``
 (the same call with 1 KiB partials), ``hot_l2`` (inputs left in L2,
 labelled), ``stream_launch`` (eager launches through the binding, no graph).
 
@@ -368,6 +369,8 @@ def run_native(args) -> None:
         extra["bandwidth"] = bandwidth_points(torch, arx, sp, dev, stream, l2)
         extra["protocol"] = protocol_point(torch, arx, sp, dev, stream, l2, args.workload)
         link = pinned_copy_gbs(torch, dev)
+        extra["protocol_host_slots"] = protocol_host_slots_point(torch, arx, sp, dev, stream, l2,
+                                                                 args.workload, link)
         extra["e2e"] = e2e_point(torch, arx, sp, dev, stream, args.workload, max(200, min(args.steps, 5000)),
                                  l2, link)
     if rank != 0:
@@ -512,6 +515,38 @@ def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:
                               "seq": seq, "reduce_model_GBs": gbs((W + 1) * n * 2, t / steps)}
     res["us_per_step"] = res["modes"]["semaphore"]["us_per_step"]
     return res
+
+
+def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link) -> dict:
+    """arx_step with the slot banks in page-locked host memory (arx_ctx_init_split):
+    every step writes the W staged partials to host memory and reads them back
+    over NVLink-C2C.  Link roofline: the time the measured pinned copy rates
+    need to move those bytes out and back."""
+    W, n = 8, sp.N_32x4096
+    x, _ = sp.workload(workload)
+    R = rotation_sets(W * n * 2 * 2, l2)
+    parts = torch.empty(R, W, n, dtype=torch.bfloat16, device=dev)
+    parts.copy_(x.to(dev).unsqueeze(0).expand(R, W, n))
+    outs = torch.empty(R, n, dtype=torch.bfloat16, device=dev)
+    lists = [[parts[k, r] for r in range(W)] for k in range(R)]
+    words = torch.zeros(arx.arx_ctx_words_bytes(W), dtype=torch.uint8, device=dev)
+    slots = torch.empty(arx.arx_ctx_slots_bytes(W, n), dtype=torch.uint8).pin_memory()
+    ctx = arx.arx_ctx_init_split(words, slots, W, n)
+
+    def call(i):
+        arx.arx_step(ctx, lists[i % R], outs[i % R], stream=stream)
+
+    steps = 2000
+    t = timed_graph_calls(torch, stream, call, steps, 10) / steps
+    st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
+    moved = W * n * 2
+    t_link = moved / (link["d2h"] * 1e9) + moved / (link["h2d"] * 1e9)
+    return {"W": W, "n": n, "steps": steps, "blocks_per_rank": ctx.nblocks, "us_per_step": t * 1e6,
+            "status": arx.arx_status_string(st), "seq": seq,
+            "link_bytes_per_step": 2 * moved,
+            "roofline": {"bound": "c2c", "link_bound_us": t_link * 1e6, "frac": t_link / t,
+                         "basis": "staged bytes out at the measured pinned D2H rate plus back at the "
+                                  "measured H2D rate, serially"}}
 
 
 def pinned_copy_gbs(torch, dev, nbytes: int = 1 << 26, reps: int = 5) -> dict:

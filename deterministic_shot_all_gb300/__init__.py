@@ -34,6 +34,7 @@ ARX_STEP_MAX_BLOCKS = 256
 ARX_DEFAULT_TIMEOUT_NS = 1_000_000_000
 ARX_NOALLOC_MAX_N = 131072
 ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED = range(3)
+ARX_SLOTS_DEVICE, ARX_SLOTS_HOST = range(2)
 
 
 class ArxError(RuntimeError):
@@ -50,7 +51,7 @@ class arx_ctx(ctypes.Structure):
         ("nblocks", ctypes.c_int32),
         ("fault_rank", ctypes.c_int32),
         ("sync_mode", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("slots_where", ctypes.c_int32),
         ("max_n", ctypes.c_uint64),
         ("slot_stride", ctypes.c_uint64),
         ("timeout_ns", ctypes.c_uint64),
@@ -61,6 +62,8 @@ class arx_ctx(ctypes.Structure):
         ("off_pad", ctypes.c_uint64),
         ("off_slots", ctypes.c_uint64),
         ("ctrl_bytes", ctypes.c_uint64),
+        ("slots", ctypes.c_void_p),
+        ("slots_bytes", ctypes.c_uint64),
     ]
 
 
@@ -81,6 +84,9 @@ def _load() -> ctypes.CDLL:
         "arx_reduce_host": ([ptrs, i32, vp, sz, vp, sz, vp], i32),
         "arx_ctx_workspace_bytes": ([i32, sz, i32], sz),
         "arx_ctx_init": ([ctxp, vp, sz, i32, sz, i32], i32),
+        "arx_ctx_words_bytes": ([i32, i32], sz),
+        "arx_ctx_slots_bytes": ([i32, sz], sz),
+        "arx_ctx_init_split": ([ctxp, vp, sz, vp, sz, i32, i32, sz, i32], i32),
         "arx_ctx_set_timeout": ([ctxp, u64], i32),
         "arx_ctx_set_fault": ([ctxp, i32], i32),
         "arx_ctx_set_sync": ([ctxp, i32], i32),
@@ -194,6 +200,27 @@ def arx_ctx_init(ws, W: int, max_n: int, nblocks: int = 0, ws_bytes: int | None 
     return ctx
 
 
+def arx_ctx_words_bytes(W: int, nblocks: int = 0) -> int:
+    return int(lib.arx_ctx_words_bytes(W, nblocks))
+
+
+def arx_ctx_slots_bytes(W: int, max_n: int) -> int:
+    return int(lib.arx_ctx_slots_bytes(W, max_n))
+
+
+def arx_ctx_init_split(words, slots, W: int, max_n: int, nblocks: int = 0) -> arx_ctx:
+    """Context with the protocol words in ``words`` (a zero-filled device tensor) and
+    the slot banks in ``slots``: a device tensor, or a page-locked host tensor
+    (``pin_memory()``), which the kernel then writes and reads over the CPU-GPU link."""
+    where = ARX_SLOTS_DEVICE if getattr(slots, "is_cuda", True) else ARX_SLOTS_HOST
+    ctx = arx_ctx()
+    _check(lib.arx_ctx_init_split(ctypes.byref(ctx), _ptr(words), words.numel() * words.element_size(),
+                                  _ptr(slots), slots.numel() * slots.element_size(), where, W, max_n,
+                                  nblocks))
+    ctx._ws_ref = (words, slots)  # keep both buffers alive as long as the context
+    return ctx
+
+
 def arx_ctx_set_timeout(ctx: arx_ctx, ns: int) -> None:
     _check(lib.arx_ctx_set_timeout(ctypes.byref(ctx), int(ns)))
 
@@ -245,6 +272,7 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
 __all__ = [
     "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce",
     "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
+    "arx_ctx_words_bytes", "arx_ctx_slots_bytes", "arx_ctx_init_split",
     "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_set_sync", "arx_ctx_reset", "arx_step", "arx_ctx_query",
     "arx_step_noalloc",
 ]

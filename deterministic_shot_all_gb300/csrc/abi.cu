@@ -255,14 +255,35 @@ size_t arx_ctx_workspace_bytes(int W, size_t max_n, int nblocks) {
   return L.total;
 }
 
-arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t max_n, int nblocks) {
+size_t arx_ctx_words_bytes(int W, int nblocks) {
+  Layout L;
+  if (!layout(W, 1, nblocks == 0 ? ARX_STEP_MAX_BLOCKS : nblocks, &L)) return 0;
+  return L.off_slots;
+}
+
+size_t arx_ctx_slots_bytes(int W, size_t max_n) {
+  Layout L;
+  if (!layout(W, max_n, 1, &L)) return 0;
+  return L.total - L.off_slots;
+}
+
+namespace {
+
+// Common part of both context initialisers: `slots` is the device address of
+// the slot banks, `slots_bytes` their capacity.
+arx_status init_ctx(arx_ctx* ctx, void* words, size_t words_bytes, bool one_buffer, void* slots,
+                    size_t slots_bytes, int slots_where, int W, size_t max_n, int nblocks) {
   if (!ctx) return fail(ARX_EINVAL, "null ctx");
   std::memset(ctx, 0, sizeof *ctx);
   if (W < 1 || W > ARX_MAX_W) return fail(ARX_EINVAL, "W=%d outside 1..%d", W, ARX_MAX_W);
   if (nblocks < 0 || nblocks > ARX_STEP_MAX_BLOCKS)
     return fail(ARX_EINVAL, "nblocks=%d outside 0..%d", nblocks, ARX_STEP_MAX_BLOCKS);
-  if (!ws) return fail(ARX_EINVAL, "null workspace");
-  if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(ARX_EINVAL, "workspace not 256-byte aligned");
+  if (!words) return fail(ARX_EINVAL, "null workspace");
+  if (reinterpret_cast<uintptr_t>(words) & 255u) return fail(ARX_EINVAL, "workspace not 256-byte aligned");
+  if (!one_buffer) {
+    if (!slots) return fail(ARX_EINVAL, "null slots buffer");
+    if (reinterpret_cast<uintptr_t>(slots) & 255u) return fail(ARX_EINVAL, "slots not 256-byte aligned");
+  }
   int B = nblocks;
   if (B == 0) {
     arx_status s = ARX_OK;
@@ -271,8 +292,22 @@ arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t m
   }
   Layout L;
   if (!layout(W, max_n, B, &L)) return fail(ARX_EINVAL, "max_n=%zu too large", max_n);
-  if (ws_bytes < L.total) return fail(ARX_EINVAL, "workspace %zu bytes, need %zu", ws_bytes, L.total);
+  if (one_buffer) {
+    if (words_bytes < L.total) return fail(ARX_EINVAL, "workspace %zu bytes, need %zu", words_bytes, L.total);
+    slots = static_cast<uint8_t*>(words) + L.off_slots;
+    slots_bytes = L.total - L.off_slots;
+  } else {
+    if (words_bytes < L.off_slots)
+      return fail(ARX_EINVAL, "words buffer %zu bytes, need %zu", words_bytes, L.off_slots);
+    if (slots_bytes < L.total - L.off_slots)
+      return fail(ARX_EINVAL, "slots buffer %zu bytes, need %zu", slots_bytes, L.total - L.off_slots);
+    if (overlap_kind(words, slots, L.off_slots, L.total - L.off_slots) != 0)
+      return fail(ARX_EOVERLAP, "words and slots buffers overlap");
+  }
   ctx->magic = kCtxMagic;
+  ctx->slots = slots;
+  ctx->slots_bytes = slots_bytes;
+  ctx->slots_where = slots_where;
   ctx->W = W;
   ctx->nblocks = B;
   ctx->fault_rank = -1;
@@ -280,14 +315,33 @@ arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t m
   ctx->max_n = max_n;
   ctx->slot_stride = L.slot_stride;
   ctx->timeout_ns = ARX_DEFAULT_TIMEOUT_NS;
-  ctx->ws = ws;
-  ctx->ws_bytes = ws_bytes;
+  ctx->ws = words;
+  ctx->ws_bytes = words_bytes;
   ctx->off_epoch = L.off_epoch;
   ctx->off_sem = L.off_sem;
   ctx->off_pad = L.off_pad;
   ctx->off_slots = L.off_slots;
   ctx->ctrl_bytes = L.off_slots;
   return ok();
+}
+
+}  // namespace
+
+arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t max_n, int nblocks) {
+  return init_ctx(ctx, ws, ws_bytes, true, nullptr, 0, ARX_SLOTS_DEVICE, W, max_n, nblocks);
+}
+
+arx_status arx_ctx_init_split(arx_ctx* ctx, void* words, size_t words_bytes, void* slots,
+                              size_t slots_bytes, int slots_where, int W, size_t max_n, int nblocks) {
+  if (slots_where == ARX_SLOTS_HOST) {
+    if (!slots) return fail(ARX_EINVAL, "null slots buffer");
+    const void* dev = pinned_device_address(slots);
+    if (!dev) return fail(ARX_EINVAL, "host slots buffer is not page-locked memory known to CUDA");
+    slots = const_cast<void*>(dev);
+  } else if (slots_where != ARX_SLOTS_DEVICE) {
+    return fail(ARX_EINVAL, "slots_where=%d is neither ARX_SLOTS_DEVICE nor ARX_SLOTS_HOST", slots_where);
+  }
+  return init_ctx(ctx, words, words_bytes, false, slots, slots_bytes, slots_where, W, max_n, nblocks);
 }
 
 arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns) {
@@ -336,6 +390,13 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   if (s != ARX_OK) return s;
   if (overlap_kind(out, ctx->ws, n * 2, ctx->ws_bytes) != 0)
     return fail(ARX_EOVERLAP, "output overlaps the workspace");
+  if (overlap_kind(out, ctx->slots, n * 2, ctx->slots_bytes) != 0)
+    return fail(ARX_EOVERLAP, "output overlaps the slots");
+  for (int r = 0; r < ctx->W; ++r) {
+    if (overlap_kind(inputs[r], ctx->ws, n * 2, ctx->ws_bytes) != 0 ||
+        overlap_kind(inputs[r], ctx->slots, n * 2, ctx->slots_bytes) != 0)
+      return fail(ARX_EOVERLAP, "input %d overlaps the workspace or the slots", r);
+  }
   cudaError_t e = cudaSuccess;
   const int cap = arx::step_capacity(ctx->W, &e);
   if (cap < 1) return fail_cuda(e, "arx_step occupancy query");
@@ -350,7 +411,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.off_epoch = ctx->off_epoch;
   c.off_sem = ctx->off_sem;
   c.off_pad = ctx->off_pad;
-  c.off_slots = ctx->off_slots;
+  c.slots = static_cast<uint16_t*>(ctx->slots);
   c.slot_stride = ctx->slot_stride;
   c.timeout_ns = ctx->timeout_ns;
   c.W = ctx->W;

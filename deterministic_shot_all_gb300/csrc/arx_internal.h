@@ -35,7 +35,8 @@ struct StepCall {
   uint16_t* out;
   size_t n;
   uint8_t* ws;
-  uint64_t off_epoch, off_sem, off_pad, off_slots, slot_stride;
+  uint16_t* slots;  // slots[2][W][slot_stride] (device address; may be page-locked host memory)
+  uint64_t off_epoch, off_sem, off_pad, slot_stride;
   uint64_t timeout_ns;
   int W, B;
   int fault_rank;

@@ -93,7 +93,8 @@ struct StepArgs {
   uint16_t* out;
   size_t n;
   uint8_t* ws;
-  uint64_t off_epoch, off_sem, off_pad, off_slots, slot_stride;
+  uint16_t* slots;
+  uint64_t off_epoch, off_sem, off_pad, slot_stride;
   uint64_t timeout_ns;
   int B;
   int fault_rank;
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   uint32_t* epoch = reinterpret_cast<uint32_t*>(a.ws + a.off_epoch);
   Semaphore* sem = reinterpret_cast<Semaphore*>(a.ws + a.off_sem);
   uint32_t* pad = reinterpret_cast<uint32_t*>(a.ws + a.off_pad);
-  uint16_t* slots = reinterpret_cast<uint16_t*>(a.ws + a.off_slots);
+  uint16_t* slots = a.slots;
   const uint32_t total_blocks = B * uint32_t(W);
 
   __shared__ uint32_t s_seq;
@@ -397,7 +398,7 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   a.off_epoch = c.off_epoch;
   a.off_sem = c.off_sem;
   a.off_pad = c.off_pad;
-  a.off_slots = c.off_slots;
+  a.slots = c.slots;
   a.slot_stride = c.slot_stride;
   a.timeout_ns = c.timeout_ns;
   a.B = c.B;

@@ -117,7 +117,7 @@ extern "C" arx_status arx_step_noalloc(const void* const* inputs, int W, void* o
   c.off_epoch = kOffEpoch;
   c.off_sem = kOffSem;
   c.off_pad = kOffPad;
-  c.off_slots = kOffSlots;
+  c.slots = reinterpret_cast<uint16_t*>(ws + kOffSlots);
   c.slot_stride = kSlotStride;
   c.timeout_ns = ARX_DEFAULT_TIMEOUT_NS;
   c.W = W;

@@ -162,7 +162,7 @@ typedef struct arx_ctx {
   int32_t nblocks;       /* B, thread blocks per virtual rank */
   int32_t fault_rank;    /* -1, or a virtual rank that skips its end-barrier signal (testing) */
   int32_t sync_mode;     /* ARX_SYNC_* (arx_ctx_set_sync); ARX_SYNC_SEMAPHORE after init */
-  int32_t reserved0;
+  int32_t slots_where;   /* ARX_SLOTS_DEVICE or ARX_SLOTS_HOST */
   uint64_t max_n;        /* capacity of one slot, elements */
   uint64_t slot_stride;  /* elements from one slot to the next (multiple of 128) */
   uint64_t timeout_ns;   /* bound of every device wait */
@@ -170,6 +170,9 @@ typedef struct arx_ctx {
   uint64_t ws_bytes;
   uint64_t off_epoch, off_sem, off_pad, off_slots;
   uint64_t ctrl_bytes;   /* bytes [0, ctrl_bytes) hold every protocol word */
+  void* slots;           /* device address of slots[2][W][slot_stride]: ws + off_slots,
+                            or the separate buffer of arx_ctx_init_split */
+  uint64_t slots_bytes;
 } arx_ctx;
 
 /* Workspace bytes for W virtual ranks, slots of max_n elements and `nblocks`
@@ -183,6 +186,31 @@ size_t arx_ctx_workspace_bytes(int W, size_t max_n, int nblocks);
  * after any step that reported an error (see arx_ctx_reset). */
 arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t max_n,
                         int nblocks);
+
+/* The same context with the protocol words and the slot banks in two
+ * buffers, so that the slots can live in page-locked host memory -- arx.cu's
+ * GB10 layout, where the send and receive slots are pinned host buffers that
+ * the GPU reads and writes directly.  On GB300 the kernel then stages every
+ * partial into host memory and reads the staged slots back over NVLink-C2C.
+ *   words        DEVICE buffer, zero-filled, 256-byte aligned, of at least
+ *                arx_ctx_words_bytes(W, nblocks) bytes: the header, epochs,
+ *                Semaphores and pad (every atomic stays in device memory).
+ *   slots        at least arx_ctx_slots_bytes(W, max_n) bytes, 256-byte
+ *                aligned, contents irrelevant:
+ *                  slots_where == ARX_SLOTS_DEVICE: a device pointer;
+ *                  slots_where == ARX_SLOTS_HOST: the HOST address of
+ *                  page-locked memory (cudaHostAlloc, cudaHostRegister,
+ *                  torch pin_memory); the library looks up its device
+ *                  address (ARX_EINVAL if it is not page-locked).
+ * Everything else as arx_ctx_init; arx_ctx_reset zeroes the words only.
+ * Buffers are the caller's and must outlive the context's last step. */
+#define ARX_SLOTS_DEVICE 0
+#define ARX_SLOTS_HOST 1
+size_t arx_ctx_words_bytes(int W, int nblocks);
+size_t arx_ctx_slots_bytes(int W, size_t max_n);
+arx_status arx_ctx_init_split(arx_ctx* ctx, void* words, size_t words_bytes, void* slots,
+                              size_t slots_bytes, int slots_where, int W, size_t max_n,
+                              int nblocks);
 
 /* Sets the bound of every device wait (ns > 0). */
 arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
@@ -220,9 +248,10 @@ arx_status arx_ctx_set_fault(arx_ctx* ctx, int rank);
 arx_status arx_ctx_reset(const arx_ctx* ctx, void* stream);
 
 /* One protocol step: out = rank-order reduce of inputs[0..W-1].
- *   inputs  HOST array of ctx->W device pointers, each to n bf16 elements.
+ *   inputs  HOST array of ctx->W device pointers, each to n bf16 elements;
+ *           none may overlap the protocol words or the slots (ARX_EOVERLAP).
  *   out     device pointer to n bf16; may equal one input exactly; must not
- *           overlap the workspace.
+ *           overlap the protocol words or the slots.
  *   n       0 < n <= ctx->max_n (n == 0 returns ARX_OK, no launch).
  * Steps on one context must be serialised (one stream, or events). */
 arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, size_t n,

@@ -152,3 +152,41 @@ def test_ctx_knobs_and_step_validation(arx):
     # Null input.
     bad = (ctypes.c_void_p * W)(*([0] + list(ins[1:])))
     assert arx.lib.arx_step(ctypes.byref(ctx), bad, FAKE + (1 << 34), n, None) == arx.ARX_EINVAL
+
+
+def test_split_layout_and_rejections(arx):
+    W, n, B = 8, 131072, 19
+    words = arx.arx_ctx_words_bytes(W, B)
+    slots = arx.arx_ctx_slots_bytes(W, n)
+    assert words + slots == arx.arx_ctx_workspace_bytes(W, n, B)
+    assert arx.arx_ctx_words_bytes(W, 0) >= words and arx.arx_ctx_words_bytes(0, B) == 0
+    assert arx.arx_ctx_slots_bytes(9, n) == 0
+    ctx = arx.arx_ctx()
+    S = FAKE + (1 << 32)
+    init = arx.lib.arx_ctx_init_split
+    assert init(ctypes.byref(ctx), FAKE, words, S, slots, arx.ARX_SLOTS_DEVICE, W, n, B) == arx.ARX_OK
+    assert ctx.slots == S and ctx.slots_bytes == slots and ctx.ctrl_bytes == words
+    assert ctx.slots_where == arx.ARX_SLOTS_DEVICE and ctx.ws == FAKE
+    assert init(ctypes.byref(ctx), FAKE, words - 1, S, slots, 0, W, n, B) == arx.ARX_EINVAL
+    assert init(ctypes.byref(ctx), FAKE, words, S, slots - 1, 0, W, n, B) == arx.ARX_EINVAL
+    assert init(ctypes.byref(ctx), FAKE, words, S + 16, slots, 0, W, n, B) == arx.ARX_EINVAL
+    assert init(ctypes.byref(ctx), FAKE, words, 0, slots, 0, W, n, B) == arx.ARX_EINVAL
+    assert init(ctypes.byref(ctx), FAKE, words, FAKE + 256, slots, 0, W, n, B) == arx.ARX_EOVERLAP
+    assert init(ctypes.byref(ctx), FAKE, words, S, slots, 2, W, n, B) == arx.ARX_EINVAL
+    # The single-buffer form places the slots right after the words.
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, words + slots, W, n, B) == arx.ARX_OK
+    assert ctx.slots == FAKE + ctx.off_slots and ctx.slots_bytes == slots
+
+
+def test_step_rejects_inputs_overlapping_the_slots(arx):
+    W, n, B = 2, 4096, 2
+    words, slots = arx.arx_ctx_words_bytes(W, B), arx.arx_ctx_slots_bytes(W, n)
+    ctx = arx.arx_ctx()
+    S = FAKE + (1 << 32)
+    assert arx.lib.arx_ctx_init_split(ctypes.byref(ctx), FAKE, words, S, slots, 0, W, n, B) == arx.ARX_OK
+    out = FAKE + (1 << 34)
+    ok_in = (ctypes.c_void_p * W)(FAKE + (1 << 35), FAKE + (1 << 35) + (1 << 20))
+    in_slots = (ctypes.c_void_p * W)(S + 512, FAKE + (1 << 35))
+    assert arx.lib.arx_step(ctypes.byref(ctx), in_slots, out, n, None) == arx.ARX_EOVERLAP
+    assert arx.lib.arx_step(ctypes.byref(ctx), ok_in, S, n, None) == arx.ARX_EOVERLAP
+    assert "slots" in arx.arx_last_error()

@@ -17,6 +17,10 @@
   ``ARX_SYNC_PAD``, ``ARX_SYNC_PAD_FENCED``: common.cuh's Semaphore barriers,
   or triton_barrier.py's pad barrier in its Patterns 0/1/2, relaxed or
   acq_rel), and switching variants between steps of one context.
+* The slot banks in a separate buffer (``arx_ctx_init_split``), in device
+  memory or in page-locked host memory (arx.cu's GB10 layout: pinned host
+  slots the GPU writes and reads over the CPU-GPU link): single steps, the
+  words against the model, the fault test and the 10,000-step graph.
 """
 
 from concurrent.futures import ThreadPoolExecutor
@@ -45,11 +49,23 @@ def dev(arx):
 class Ctx:
     """A context plus typed views of its workspace words."""
 
-    def __init__(self, arx, dev, W, max_n, nblocks=0, sync="semaphore"):
+    def __init__(self, arx, dev, W, max_n, nblocks=0, sync="semaphore", slots="one"):
+        """slots: "one" (words and slots in one device buffer), "device" or "host"
+        (separate slot buffer in device memory or in page-locked host memory)."""
         self.arx = arx
-        nbytes = arx.arx_ctx_workspace_bytes(W, max_n, nblocks)
-        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
-        self.ctx = arx.arx_ctx_init(self.ws, W, max_n, nblocks)
+        self.where = slots
+        if slots == "one":
+            nbytes = arx.arx_ctx_workspace_bytes(W, max_n, nblocks)
+            self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+            self.ctx = arx.arx_ctx_init(self.ws, W, max_n, nblocks)
+        else:
+            self.ws = torch.zeros(arx.arx_ctx_words_bytes(W, nblocks), dtype=torch.uint8, device=dev)
+            sb = arx.arx_ctx_slots_bytes(W, max_n)
+            # Fill the slots with garbage: their contents must not matter.
+            self.slots = torch.full((sb,), 0xA5, dtype=torch.uint8)
+            self.slots = self.slots.pin_memory() if slots == "host" else self.slots.to(dev)
+            self.ctx = arx.arx_ctx_init_split(self.ws, self.slots, W, max_n, nblocks)
+            assert self.ctx.slots_where == (arx.ARX_SLOTS_HOST if slots == "host" else arx.ARX_SLOTS_DEVICE)
         self.W, self.B = W, self.ctx.nblocks
         self.set_sync(sync)
 
@@ -71,8 +87,12 @@ class Ctx:
 
     def slot(self, par, r, n):
         c = self.ctx
-        off = c.off_slots + (par * self.W + r) * c.slot_stride * 2
-        return self.ws[off: off + 2 * n].cpu().numpy().view(np.uint16)
+        off = (par * self.W + r) * c.slot_stride * 2
+        if self.where == "one":
+            off += c.off_slots
+            return self.ws[off: off + 2 * n].cpu().numpy().view(np.uint16)
+        torch.cuda.synchronize()
+        return self.slots[off: off + 2 * n].cpu().numpy().view(np.uint16)
 
     def poke(self, off, value):
         self.ws[off: off + 4] = torch.tensor([value], dtype=torch.int64).view(torch.uint8)[:4].to(self.ws.device)
@@ -116,6 +136,21 @@ def test_single_step_every_w(arx, dev, W, sync):
                           f"step W={W} n={n} B={c.B}")
 
 
+@pytest.mark.parametrize("W", [1, 2, 5, 8])
+def test_single_step_host_slots(arx, dev, W):
+    # The slot banks in page-locked host memory: staged partials go out over
+    # the CPU-GPU link and are read back from there.
+    for n, nblocks in ((131072, 0), (1000003, 0), (13, 1), (4096 + 5, 3)):
+        c = Ctx(arx, dev, W, n, nblocks, "semaphore", "host")
+        x = sp.partials(W, n, "special" if n < 5000 else "normal", seed=W * 11 + n)
+        out = _step(arx, c, x, dev)
+        st, seq, err = arx.arx_ctx_query(c.ctx)
+        assert (st, seq, err) == (arx.ARX_OK, 1, 0)
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                          f"host slots W={W} n={n} B={c.B}")
+        assert np.array_equal(c.slot(1, W - 1, n), sp.to_u16_numpy(x)[W - 1])
+
+
 def test_step_equals_stateless_reduce(arx, dev):
     x, _ = sp.workload("w8_32x4096_normal")
     xd = x.to(dev)
@@ -151,10 +186,11 @@ def test_step_output_aliases_an_input(arx, dev):
                       oracle.reduce(list(sp.to_u16_numpy(x))), "step in place")
 
 
+@pytest.mark.parametrize("slots", ["one", "device", "host"])
 @pytest.mark.parametrize("sync", SYNCS)
 @pytest.mark.parametrize("W,n,B,k", [(8, 131072, 0, 5), (3, 777, 2, 4), (5, 65536 + 7, 7, 3), (1, 100, 1, 2)])
-def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync):
-    c = Ctx(arx, dev, W, n, B, sync)
+def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync, slots):
+    c = Ctx(arx, dev, W, n, B, sync, slots)
     st = model.State(W=W, B=c.B)
     hist = []
     for s in range(k):
@@ -199,10 +235,10 @@ def test_unsigned_wrap_of_seq_and_flags(arx, dev):
     assert w["seq"] == 1
 
 
-@pytest.mark.parametrize("sync", SYNCS)
-def test_timeout_is_reported_and_context_recovers(arx, dev, sync):
+@pytest.mark.parametrize("sync,slots", [(m, "one") for m in SYNCS] + [("semaphore", "host")])
+def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
     W, n = 4, 8192
-    c = Ctx(arx, dev, W, n, 2, sync)
+    c = Ctx(arx, dev, W, n, 2, sync, slots)
     x = sp.partials(W, n, "normal", seed=8)
     _step(arx, c, x, dev)
     assert arx.arx_ctx_query(c.ctx)[:2] == (arx.ARX_OK, 1)
@@ -297,11 +333,11 @@ def graph_workload(dev):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("sync", SYNCS)
-def test_ten_thousand_steps_in_one_graph(arx, dev, graph_workload, sync):
+@pytest.mark.parametrize("sync,slots", [(m, "one") for m in SYNCS] + [("semaphore", "host")])
+def test_ten_thousand_steps_in_one_graph(arx, dev, graph_workload, sync, slots):
     inputs, want, last_two = graph_workload
     steps = inputs.shape[0]
-    c = Ctx(arx, dev, W8, N8, 0, sync)
+    c = Ctx(arx, dev, W8, N8, 0, sync, slots)
     outputs = torch.zeros(steps, N8, dtype=torch.bfloat16, device=dev)
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
