@@ -24,7 +24,8 @@ same metric through ``arx_reduce_host`` with pinned host buffers, the
 partials crossing the CPU-GPU link every call, against the link's measured
 pinned copy rate), ``bandwidth`` (bandwidth-bound sizes: W=4 [1024, 8192] in
 place, W=8 at 16 MiB and 256 MiB per partial), ``protocol`` (``arx_step``
-per step in a captured graph, for each barrier variant), ``protocol_host_slots``
+per step in a captured graph, for each barrier variant), ``protocol_graph``
+(10,000 steps with fresh partials captured in one CUDA graph), ``protocol_host_slots``
 (the step with its slot banks in page-locked host memory), ``latency_floor``
 (the same call with 1 KiB partials), ``hot_l2`` (inputs left in L2,
 labelled), ``stream_launch`` (eager launches through the binding, no graph).
@@ -368,6 +369,7 @@ def run_native(args) -> None:
         extra["stream_launch"] = stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R)
         extra["bandwidth"] = bandwidth_points(torch, arx, sp, dev, stream, l2)
         extra["protocol"] = protocol_point(torch, arx, sp, dev, stream, l2, args.workload)
+        extra["protocol_graph"] = protocol_graph_point(torch, arx, sp, dev, stream)
         link = pinned_copy_gbs(torch, dev)
         extra["protocol_host_slots"] = protocol_host_slots_point(torch, arx, sp, dev, stream, l2,
                                                                  args.workload, link)
@@ -514,6 +516,52 @@ def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:
         res["modes"][mode] = {"us_per_step": t / steps * 1e6, "status": arx.arx_status_string(st),
                               "seq": seq, "reduce_model_GBs": gbs((W + 1) * n * 2, t / steps)}
     res["us_per_step"] = res["modes"]["semaphore"]["us_per_step"]
+    return res
+
+
+def protocol_graph_point(torch, arx, sp, dev, stream) -> dict:
+    """The graph workload as specified: W = 8 bf16 [32, 4096], GRAPH_STEPS (10,000)
+    arx_step calls captured in ONE CUDA graph, fresh normal(0, 1) partials for
+    every step (a [10000][8][n] device array, 21 GB, far beyond L2), one output
+    per step.  The partials are drawn on the device here (timing only; the
+    tests check every step bit for bit with the CPU-drawn seeds 4 + step).
+    µs/step = graph replay time / steps."""
+    W, n, steps = 8, sp.N_32x4096, sp.GRAPH_STEPS
+    inputs = torch.empty(steps, W, n, dtype=torch.bfloat16, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(4)
+    for lo in range(0, steps, 1000):
+        hi = min(steps, lo + 1000)
+        inputs[lo:hi] = torch.randn((hi - lo, W, n), generator=gen, device=dev).to(torch.bfloat16)
+    outputs = torch.empty(steps, n, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
+    ctx = arx.arx_ctx_init(ws, W, n)
+    lists = [[inputs[t, r] for r in range(W)] for t in range(steps)]
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    t0 = time.perf_counter()
+    with torch.cuda.graph(g, stream=stream):
+        for t in range(steps):
+            arx.arx_step(ctx, lists[t], outputs[t], stream=stream)
+    capture_s = time.perf_counter() - t0
+    times = []
+    with torch.cuda.stream(stream):
+        g.replay()                      # warm-up replay (untimed)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            g.replay()
+            e.record(stream)
+            torch.cuda.synchronize()
+            times.append(s.elapsed_time(e) / 1e3)
+    st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
+    t = statistics.median(times)
+    res = {"W": W, "n": n, "steps_per_graph": steps, "replays": len(times), "us_per_step": t / steps * 1e6,
+           "graph_ms": t * 1e3, "capture_s": capture_s, "status": arx.arx_status_string(st),
+           "seq": seq, "blocks_per_rank": ctx.nblocks}
+    del g, inputs, outputs, lists
+    torch.cuda.empty_cache()
     return res
 
 

@@ -26,6 +26,8 @@
 //    between back-to-back calls.
 // The launch policy (threads, U, kPipe per W and size) comes from a measured
 // sweep of these shapes on GB300.
+#include <atomic>
+
 #include "arx_device.cuh"
 #include "arx_internal.h"
 
@@ -174,12 +176,15 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const VecArgs a
 constexpr int kMaxDevices = 64;
 
 template <typename Kernel>
-int blocks_per_sm(Kernel k, int threads, int dev, int* cache, cudaError_t* err) {
-  if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+int blocks_per_sm(Kernel k, int threads, int dev, std::atomic<int>* cache, cudaError_t* err) {
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int b = 0;
   *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, threads, 0);
   if (*err != cudaSuccess || b < 1) return -1;
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = b;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(b, std::memory_order_relaxed);
   return b;
 }
 
@@ -202,7 +207,7 @@ cudaError_t launch_dependent(Kernel k, size_t blocks, int threads, cudaStream_t 
 
 template <int W, int T, int U, bool kPipe, bool kAlias>
 cudaError_t launch_vec(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
-  static int cache[kMaxDevices];
+  static std::atomic<int> cache[kMaxDevices];
   cudaError_t err = cudaSuccess;
   auto k = reduce_vec_kernel<W, T, U, kPipe, kAlias>;
   const int per_sm = blocks_per_sm(k, T, dev, cache, &err);
@@ -217,7 +222,7 @@ cudaError_t launch_vec(const VecArgs& a, int dev, int sms, cudaStream_t stream) 
 
 template <int W, int T, bool kAlias>
 cudaError_t launch_half(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
-  static int cache[kMaxDevices];
+  static std::atomic<int> cache[kMaxDevices];
   cudaError_t err = cudaSuccess;
   auto k = reduce_half_kernel<W, T, kAlias>;
   const int per_sm = blocks_per_sm(k, T, dev, cache, &err);
@@ -291,15 +296,18 @@ cudaError_t launch_w(const ReduceCall& c, cudaStream_t stream) {
 }  // namespace
 
 int current_sm_count(cudaError_t* err) {
-  static int cache[kMaxDevices];
+  static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return -1;
-  if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int sms = 0;
   *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (*err != cudaSuccess || sms < 1) return -1;
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = sms;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 

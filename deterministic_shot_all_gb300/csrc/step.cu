@@ -53,6 +53,8 @@
 // by the kernel boundary) and by the host after a synchronisation, never by
 // another block of the same launch.  The pages fence there because a host
 // proxy and remote GPUs observe those words while the kernel runs.
+#include <atomic>
+
 #include "arx_device.cuh"
 #include "arx_internal.h"
 
@@ -372,8 +374,11 @@ constexpr int kMaxDevices = 64;
 // sync modes, so one capacity serves every mode.
 template <int W>
 int blocks_per_sm(int dev, cudaError_t* err) {
-  static int cache[kMaxDevices];
-  if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  static std::atomic<int> cache[kMaxDevices];  // per-device results, shared by host threads
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int lo = 0;
   const void* kernels[3] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad>),
@@ -384,7 +389,7 @@ int blocks_per_sm(int dev, cudaError_t* err) {
     if (*err != cudaSuccess || b < 1) return -1;
     lo = lo == 0 || b < lo ? b : lo;
   }
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = lo;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(lo, std::memory_order_relaxed);
   return lo;
 }
 
