@@ -127,6 +127,39 @@ def _ptr(x) -> int:
     raise TypeError(f"expected a tensor or an integer address, got {type(x).__name__}")
 
 
+def _check_bf16(xs: Sequence, n: int | None, where: str, what: str) -> None:
+    """Marshalling checks of tensor arguments (integer addresses pass unchecked):
+    bf16, contiguous, at least n elements, and on the side the call expects --
+    ``where`` is "cuda" (the current device) or "cpu".  Catches a host tensor
+    handed to a device entry point, or a wrong dtype, before any kernel sees
+    the pointer."""
+    import torch
+    current = None
+    for i, x in enumerate(xs):
+        if isinstance(x, int) or not hasattr(x, "dtype"):
+            continue
+        ok = (x.dtype == torch.bfloat16 and x.is_contiguous() and (n is None or x.numel() >= n)
+              and x.is_cuda == (where == "cuda"))
+        if ok and where == "cuda":
+            if current is None:
+                current = torch.cuda.current_device()
+            ok = x.device.index == current
+        if ok:
+            continue
+        name = f"{what}[{i}]" if len(xs) > 1 else what
+        if x.dtype != torch.bfloat16:
+            raise TypeError(f"{name}: expected torch.bfloat16, got {x.dtype}")
+        if not x.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous")
+        if n is not None and x.numel() < n:
+            raise ValueError(f"{name}: {x.numel()} elements, the call needs {n}")
+        if where == "cuda" and not x.is_cuda:
+            raise ValueError(f"{name}: expected a CUDA tensor, got one on {x.device}")
+        if where != "cuda" and x.is_cuda:
+            raise ValueError(f"{name}: expected a host (CPU) tensor, got one on {x.device}")
+        raise ValueError(f"{name}: on {x.device}, but the current device is cuda:{current}")
+
+
 def _ptr_array(xs: Sequence) -> ctypes.Array:
     return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
 
@@ -155,7 +188,10 @@ def arx_reduce(slots: Sequence, out, n: int | None = None, stream=None, check: b
     tensor or address, may be one of the slots.  Returns the arx_status (and
     raises ArxError on failure when ``check``).
     """
-    st = lib.arx_reduce(_ptr_array(slots), len(slots), _ptr(out), _numel(n, out), _stream(stream))
+    n = _numel(n, out)
+    _check_bf16(slots, n, "cuda", "slots")
+    _check_bf16([out], n, "cuda", "out")
+    st = lib.arx_reduce(_ptr_array(slots), len(slots), _ptr(out), n, _stream(stream))
     if check:
         _check(st)
     return st
@@ -176,11 +212,16 @@ def arx_reduce_host(host_slots: Sequence, host_out, staging=None, n: int | None 
     if staging is None:
         sptr, nb = None, 0
     elif hasattr(staging, "numel"):
+        if not staging.is_cuda:
+            raise ValueError("staging must be a CUDA tensor")
         sptr, nb = (staging.data_ptr() or None), staging.numel() * staging.element_size()
     else:
         raise TypeError("staging must be a device tensor or None")
+    n = _numel(n, host_out)
+    _check_bf16(host_slots, n, "cpu", "host_slots")
+    _check_bf16([host_out], n, "cpu", "host_out")
     st = lib.arx_reduce_host(_ptr_array(host_slots), len(host_slots), _ptr(host_out),
-                             _numel(n, host_out), sptr, nb, _stream(stream))
+                             n, sptr, nb, _stream(stream))
     if check:
         _check(st)
     return st
@@ -192,6 +233,8 @@ def arx_ctx_workspace_bytes(W: int, max_n: int, nblocks: int = 0) -> int:
 
 def arx_ctx_init(ws, W: int, max_n: int, nblocks: int = 0, ws_bytes: int | None = None) -> arx_ctx:
     """Context for the protocol step over a zero-filled device workspace ``ws``."""
+    if hasattr(ws, "is_cuda") and not ws.is_cuda:
+        raise ValueError("the workspace must be a CUDA tensor")
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size()
     ctx = arx_ctx()
@@ -212,6 +255,8 @@ def arx_ctx_init_split(words, slots, W: int, max_n: int, nblocks: int = 0) -> ar
     """Context with the protocol words in ``words`` (a zero-filled device tensor) and
     the slot banks in ``slots``: a device tensor, or a page-locked host tensor
     (``pin_memory()``), which the kernel then writes and reads over the CPU-GPU link."""
+    if not getattr(words, "is_cuda", True):
+        raise ValueError("the protocol words must be a CUDA tensor")
     where = ARX_SLOTS_DEVICE if getattr(slots, "is_cuda", True) else ARX_SLOTS_HOST
     ctx = arx_ctx()
     _check(lib.arx_ctx_init_split(ctypes.byref(ctx), _ptr(words), words.numel() * words.element_size(),
@@ -241,7 +286,10 @@ def arx_ctx_reset(ctx: arx_ctx, stream=None) -> None:
 def arx_step(ctx: arx_ctx, inputs: Sequence, out, n: int | None = None, stream=None,
              check: bool = True) -> int:
     """Enqueue one protocol step: out = rank-order reduce of ``inputs``."""
-    st = lib.arx_step(ctypes.byref(ctx), _ptr_array(inputs), _ptr(out), _numel(n, out), _stream(stream))
+    n = _numel(n, out)
+    _check_bf16(inputs, n, "cuda", "inputs")
+    _check_bf16([out], n, "cuda", "out")
+    st = lib.arx_step(ctypes.byref(ctx), _ptr_array(inputs), _ptr(out), n, _stream(stream))
     if check:
         _check(st)
     return st
@@ -262,7 +310,10 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
     ``dev_status``: optional device int32/uint32 tensor (or address) that
     receives the step's device error word.  n is limited to ARX_NOALLOC_MAX_N.
     """
-    st = lib.arx_step_noalloc(_ptr_array(inputs), len(inputs), _ptr(out), _numel(n, out),
+    n = _numel(n, out)
+    _check_bf16(inputs, n, "cuda", "inputs")
+    _check_bf16([out], n, "cuda", "out")
+    st = lib.arx_step_noalloc(_ptr_array(inputs), len(inputs), _ptr(out), n,
                               _ptr(dev_status) if dev_status is not None else None, _stream(stream))
     if check:
         _check(st)

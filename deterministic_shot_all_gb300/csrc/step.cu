@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   if constexpr (!kPad) {
     // PullController start stage, unfenced: no block barrier before the signal.
     if (lane == 0 && warp < uint32_t(W)) {
-      atom_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
+      red_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
       if (warp == r) {
         base = own.counter;
         if (!semaphore_wait<false>(&own.flag, base, uint32_t(W), a.timeout_ns))
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   } else if (lane == 0 && warp < uint32_t(W)) {
     if (int(r) != a.fault_rank) {
       __threadfence();
-      atom_add_release_gpu(&sem[warp * B + b].flag, 1u);
+      red_add_release_gpu(&sem[warp * B + b].flag, 1u);
     }
     if (warp == r) {
       if (semaphore_wait<true>(&own.flag, base, 2u * uint32_t(W), a.timeout_ns)) {

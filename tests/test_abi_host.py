@@ -190,3 +190,26 @@ def test_step_rejects_inputs_overlapping_the_slots(arx):
     assert arx.lib.arx_step(ctypes.byref(ctx), in_slots, out, n, None) == arx.ARX_EOVERLAP
     assert arx.lib.arx_step(ctypes.byref(ctx), ok_in, S, n, None) == arx.ARX_EOVERLAP
     assert "slots" in arx.arx_last_error()
+
+
+def test_binding_rejects_tensors_of_the_wrong_kind(arx):
+    # Checked in the binding before any pointer reaches the library.
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)              # host tensors
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        arx.arx_reduce([x[0], x[1]], x[0])
+    f = torch.zeros(2, 64, dtype=torch.float32)
+    with pytest.raises(TypeError, match="bfloat16"):
+        arx.arx_reduce([f[0], f[1]], f[0])
+    t = torch.zeros(64, 2, dtype=torch.bfloat16).t()          # non-contiguous rows
+    with pytest.raises(ValueError, match="contiguous"):
+        arx.arx_reduce([t[0], t[1]], x[0])
+    with pytest.raises(ValueError, match="elements"):
+        arx.arx_reduce([x[0][:10], x[1]], x[0])
+    ws = torch.zeros(arx.arx_ctx_workspace_bytes(2, 64, 1), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        arx.arx_ctx_init(ws, 2, 64, 1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        arx.arx_step_noalloc([x[0], x[1]], x[0])
+    with pytest.raises(TypeError, match="bfloat16"):
+        arx.arx_reduce_host([f[0], f[1]], f[0])
