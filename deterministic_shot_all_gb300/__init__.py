@@ -43,6 +43,18 @@ class ArxError(RuntimeError):
         self.status = status
 
 
+class arx_watch_report(ctypes.Structure):
+    """Mirror of ``struct arx_watch_report`` in include/arx.h."""
+    _fields_ = [
+        ("seq", ctypes.c_uint32),
+        ("published", ctypes.c_uint32),
+        ("dev_err", ctypes.c_uint32),
+        ("polls", ctypes.c_uint32),
+        ("stalled_ns", ctypes.c_uint64),
+        ("waited_ns", ctypes.c_uint64),
+    ]
+
+
 class arx_ctx(ctypes.Structure):
     """Mirror of ``struct arx_ctx`` in include/arx.h."""
     _fields_ = [
@@ -94,6 +106,7 @@ def _load() -> ctypes.CDLL:
         "arx_step": ([ctxp, ptrs, vp, sz, vp], i32),
         "arx_ctx_query": ([ctxp, u32p, u32p, vp], i32),
         "arx_step_noalloc": ([ptrs, i32, vp, sz, vp, vp], i32),
+        "arx_watch_step": ([ctxp, ctypes.c_uint32, u64, u64, u64, u32p, vp, ctypes.POINTER(arx_watch_report)], i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -303,6 +316,26 @@ def arx_ctx_query(ctx: arx_ctx, stream=None) -> tuple[int, int, int]:
     return st, seq.value, err.value
 
 
+def arx_watch_step(ctx: arx_ctx, target_seq: int, stall_s: float, poll_s: float = 1e-3,
+                   max_wait_s: float = 10.0, host_words=None, stream=None) -> tuple[int, arx_watch_report]:
+    """Block until the context's completed seq reaches ``target_seq``, a staged
+    step stays not done for ``stall_s`` (a stall), or the device reports an
+    error.  Polls on ``stream`` (default: a fresh non-blocking side stream),
+    never on the steps' stream; ctypes releases the GIL for the call, so run
+    it on a thread of your own.  Returns (status, report)."""
+    import torch
+    if host_words is None:
+        host_words = torch.zeros(8, dtype=torch.int32).pin_memory()
+    if stream is None:
+        stream = torch.cuda.Stream()
+    rep = arx_watch_report()
+    st = lib.arx_watch_step(ctypes.byref(ctx), int(target_seq) & 0xFFFFFFFF, int(stall_s * 1e9),
+                            int(poll_s * 1e9), int(max_wait_s * 1e9),
+                            ctypes.cast(_ptr(host_words), ctypes.POINTER(ctypes.c_uint32)),
+                            _stream(stream), ctypes.byref(rep))
+    return st, rep
+
+
 def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=None, stream=None,
                      check: bool = True) -> int:
     """Enqueue one protocol step whose workspace is the library's static array (no allocation).
@@ -325,5 +358,5 @@ __all__ = [
     "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
     "arx_ctx_words_bytes", "arx_ctx_slots_bytes", "arx_ctx_init_split",
     "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_set_sync", "arx_ctx_reset", "arx_step", "arx_ctx_query",
-    "arx_step_noalloc",
+    "arx_step_noalloc", "arx_watch_step", "arx_watch_report",
 ]

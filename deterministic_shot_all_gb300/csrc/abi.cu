@@ -5,9 +5,11 @@
 // and drops its 512 KB / multiple-of-8 limits.
 #include <cuda_runtime.h>
 
+#include <chrono>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <thread>
 
 #include "arx.h"
 #include "arx_internal.h"
@@ -439,6 +441,72 @@ arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, v
     return fail(static_cast<arx_status>(code), "device error word 0x%08x (stage %u, rank %u, block %u)",
                 words[1], (words[1] >> 8) & 15u, (words[1] >> 12) & 15u, words[1] >> 16);
   return fail(ARX_ESTATE, "device error word 0x%08x", words[1]);
+}
+
+arx_status arx_watch_step(const arx_ctx* ctx, uint32_t target_seq, uint64_t stall_ns,
+                          uint64_t poll_ns, uint64_t max_wait_ns, uint32_t* host_words,
+                          void* stream, arx_watch_report* report) {
+  arx_watch_report rep{};
+  if (report) *report = rep;
+  const arx_status s = check_ctx(ctx);
+  if (s != ARX_OK) return s;
+  if (!host_words) return fail(ARX_EINVAL, "null host_words");
+  if (poll_ns == 0 || stall_ns == 0 || max_wait_ns == 0)
+    return fail(ARX_EINVAL, "poll, stall and max-wait times must be > 0");
+  using clock = std::chrono::steady_clock;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const auto t0 = clock::now();
+  auto since = [](clock::time_point a) {
+    return uint64_t(std::chrono::duration_cast<std::chrono::nanoseconds>(clock::now() - a).count());
+  };
+  bool gap = false;
+  clock::time_point gap_start = t0;
+  arx_status result = ARX_OK;
+  for (;;) {
+    // Header: seq (completed), err, blocks[2], published.
+    cudaError_t e = cudaMemcpyAsync(host_words, ctx->ws, 5 * sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+      result = fail_cuda(e, "arx_watch_step header copy");
+      break;
+    }
+    ++rep.polls;
+    rep.seq = host_words[0];
+    rep.dev_err = host_words[1];
+    rep.published = host_words[4];
+    const uint32_t code = rep.dev_err & 0xFFu;
+    if (code != 0) {
+      result = fail(code == ARX_ETIMEOUT ? ARX_ETIMEOUT : ARX_ESTATE,
+                    "device error word 0x%08x during the step", rep.dev_err);
+      break;
+    }
+    if (int32_t(rep.seq - target_seq) >= 0) break;  // done (unsigned wrap aware)
+    if (rep.published != rep.seq) {
+      if (!gap) {
+        gap = true;
+        gap_start = clock::now();
+      }
+      rep.stalled_ns = since(gap_start);
+      if (rep.stalled_ns >= stall_ns) {
+        result = fail(ARX_ETIMEOUT, "STALL: step %u published, completed %u, for %llu ns", rep.published,
+                      rep.seq, static_cast<unsigned long long>(rep.stalled_ns));
+        break;
+      }
+    } else {
+      gap = false;
+      rep.stalled_ns = 0;
+    }
+    if (since(t0) >= max_wait_ns) {
+      result = fail(ARX_ETIMEOUT, "completed seq %u did not reach %u within %llu ns", rep.seq, target_seq,
+                    static_cast<unsigned long long>(max_wait_ns));
+      break;
+    }
+    std::this_thread::sleep_for(std::chrono::nanoseconds(poll_ns));
+  }
+  rep.waited_ns = since(t0);
+  if (report) *report = rep;
+  if (result == ARX_OK) return ok();
+  return result;
 }
 
 }  // extern "C"

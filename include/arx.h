@@ -263,6 +263,40 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
 arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Host-side watchdog of the protocol step (arx.cu's proxy watchdog: a step
+ * published but not done for too long is reported once as a stall).
+ *
+ * arx_watch_step polls the context's header words -- completed seq,
+ * device error word, published seq -- by a small device-to-host copy on
+ * `stream` every poll_ns, without synchronising the stream the steps run on
+ * (pass a different, non-blocking stream).  It returns:
+ *   ARX_OK        once completed seq has reached target_seq (modulo 2^32);
+ *   ARX_ETIMEOUT  if a staged step stays not done (published != completed)
+ *                 for stall_ns -- typically while the step kernel is still
+ *                 inside its own bounded wait, so the stall is seen before
+ *                 the device reports it -- or if max_wait_ns passes first;
+ *   ARX_ETIMEOUT / ARX_ESTATE as soon as the device error word is set (its
+ *                 low byte);
+ *   ARX_EINVAL / ARX_ESTATE / ARX_ECUDA for bad arguments or a failed copy.
+ *   host_words   page-locked host memory for 8 uint32 (the copy target).
+ *   report       filled on return (may be NULL).
+ * It blocks the calling thread: run it on a thread of your own while steps
+ * are enqueued elsewhere.  It only reads; it never touches the GPU's work.
+ * ------------------------------------------------------------------------- */
+typedef struct arx_watch_report {
+  uint32_t seq;         /* completed steps at the last poll */
+  uint32_t published;   /* last staged step at the last poll */
+  uint32_t dev_err;     /* device error word at the last poll */
+  uint32_t polls;
+  uint64_t stalled_ns;  /* how long published != completed had lasted */
+  uint64_t waited_ns;   /* time spent in the call */
+} arx_watch_report;
+
+arx_status arx_watch_step(const arx_ctx* ctx, uint32_t target_seq, uint64_t stall_ns,
+                          uint64_t poll_ns, uint64_t max_wait_ns, uint32_t* host_words,
+                          void* stream, arx_watch_report* report);
+
+/* ---------------------------------------------------------------------------
  * Allocation-free protocol step.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory at the time
  * they call: a serving engine that reserved nearly all of HBM for its own pool

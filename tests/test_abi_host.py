@@ -213,3 +213,17 @@ def test_binding_rejects_tensors_of_the_wrong_kind(arx):
         arx.arx_step_noalloc([x[0], x[1]], x[0])
     with pytest.raises(TypeError, match="bfloat16"):
         arx.arx_reduce_host([f[0], f[1]], f[0])
+
+
+def test_watchdog_argument_checks(arx):
+    ctx = arx.arx_ctx()
+    words = (ctypes.c_uint32 * 8)()
+    rep = arx.arx_watch_report()
+    w = arx.lib.arx_watch_step
+    assert w(ctypes.byref(ctx), 1, 10**6, 10**5, 10**9, words, None, ctypes.byref(rep)) == arx.ARX_ESTATE
+    n = arx.arx_ctx_workspace_bytes(2, 64, 1)
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, n, 2, 64, 1) == arx.ARX_OK
+    assert w(ctypes.byref(ctx), 1, 10**6, 10**5, 10**9, None, None, ctypes.byref(rep)) == arx.ARX_EINVAL
+    assert w(ctypes.byref(ctx), 1, 0, 10**5, 10**9, words, None, ctypes.byref(rep)) == arx.ARX_EINVAL
+    assert w(ctypes.byref(ctx), 1, 10**6, 0, 10**9, words, None, ctypes.byref(rep)) == arx.ARX_EINVAL
+    assert w(ctypes.byref(ctx), 1, 10**6, 10**5, 0, words, None, None) == arx.ARX_EINVAL

@@ -263,6 +263,48 @@ def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
                       "after reset")
 
 
+def test_host_watchdog_reports_a_stall_before_the_device_bound(arx, dev):
+    # arx.cu's proxy watchdog, on the host: a step published but not done for
+    # longer than the stall threshold is reported while the kernel is still
+    # inside its own bounded wait.  The stall comes from the in-protocol fault
+    # (a virtual rank skips its end signal); no GPU fault is involved.
+    import threading
+    W, n = 4, 8192
+    c = Ctx(arx, dev, W, n, 2)
+    x = sp.partials(W, n, "normal", seed=8)
+    res = {}
+
+    def watch(key, target):
+        res[key] = arx.arx_watch_step(c.ctx, target, stall_s=0.05, poll_s=0.001, max_wait_s=5.0)
+
+    th = threading.Thread(target=watch, args=("ok", 1))
+    th.start()
+    _step(arx, c, x, dev)
+    th.join()
+    st, rep = res["ok"]
+    assert st == arx.ARX_OK and rep.seq == 1 and rep.dev_err == 0 and rep.polls >= 1
+
+    arx.arx_ctx_set_timeout(c.ctx, 600_000_000)     # device bound: 600 ms
+    arx.arx_ctx_set_fault(c.ctx, 1)
+    th = threading.Thread(target=watch, args=("stall", 2))
+    th.start()
+    _step(arx, c, x, dev)
+    th.join()
+    st, rep = res["stall"]
+    assert st == arx.ARX_ETIMEOUT
+    assert rep.published == 2 and rep.seq == 1 and rep.dev_err == 0
+    assert rep.stalled_ns >= 50_000_000 and rep.waited_ns < 600_000_000
+    # The device then reports its own expired wait, and the context recovers.
+    st, seq, err = arx.arx_ctx_query(c.ctx)
+    assert st == arx.ARX_ETIMEOUT and seq == 2
+    arx.arx_ctx_set_fault(c.ctx, -1)
+    arx.arx_ctx_reset(c.ctx)
+    out = _step(arx, c, x, dev)
+    assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, 1, 0)
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                      "after the stall")
+
+
 def test_epoch_mismatch_reports_state_error(arx, dev):
     W, n = 2, 1024
     c = Ctx(arx, dev, W, n, 2)
