@@ -490,7 +490,7 @@ def floor_point(torch, arx, dev, stream, l2, W, n, per_call) -> dict:
 SYNC_MODES = ("semaphore", "pad", "pad_fenced")
 
 
-def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:
+def protocol_point(torch, arx, sp, dev, stream, l2, workload, steps: int = 2000) -> dict:
     """arx_step per step (W=8, [32,4096]) in captured graphs, fresh input sets rotating,
     for each barrier variant (Semaphore barriers; pad barrier Patterns 0/1/2; all acq_rel)."""
     W, n = 8, sp.N_32x4096
@@ -500,7 +500,6 @@ def protocol_point(torch, arx, sp, dev, stream, l2, workload) -> dict:
     parts.copy_(x.to(dev).unsqueeze(0).expand(R, W, n))
     outs = torch.empty(R, n, dtype=torch.bfloat16, device=dev)
     lists = [[parts[k, r] for r in range(W)] for k in range(R)]
-    steps = 2000
     res = {"W": W, "n": n, "steps": steps, "modes": {}}
     for mode_index, mode in enumerate(SYNC_MODES):
         ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
@@ -748,6 +747,20 @@ def run_sweep(args) -> None:
                       "points": pts}), flush=True)
 
 
+def run_protocol(args) -> None:
+    """Only the protocol step (W = 8 bf16 [32, 4096], every barrier variant, --steps
+    steps each in graphs); prints one JSON object.  Used to profile the step kernel."""
+    import torch
+    import deterministic_shot_all_gb300 as arx
+    import synthetic_partials as sp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2**20)
+    stream = torch.cuda.Stream(device=dev)
+    res = protocol_point(torch, arx, sp, dev, stream, l2, DEFAULT_WORKLOAD, steps=args.steps)
+    print(json.dumps({"protocol": res}), flush=True)
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -765,6 +778,7 @@ def main(argv=None) -> None:
     p.add_argument("--sweep-w", type=int, default=8)
     p.add_argument("--sweep-min", type=int, default=9)
     p.add_argument("--sweep-max", type=int, default=27)
+    p.add_argument("--protocol", action="store_true", help="only the protocol step, every barrier variant")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -772,6 +786,8 @@ def main(argv=None) -> None:
         p.error("--steps must be >= 1")
     if args.sweep:
         run_sweep(args)
+    elif args.protocol:
+        run_protocol(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
