@@ -224,6 +224,24 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     if (epoch_in != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
 
+  // Chunk b (in 16-byte groups) and the first batch of this block's staging
+  // loads.  They read only the caller's input, which no barrier guards, so
+  // they are issued before the start barrier and their DRAM latency overlaps
+  // it; the slot writes still wait for the barrier.
+  const size_t G = a.n / 8u;
+  const size_t tail = a.n - 8u * G;
+  const size_t c0 = split_point(G, B, b), c1 = split_point(G, B, b + 1u);
+  const bool in_vec = (a.in_vec_mask >> r) & 1u;
+  const uint4* s4 = reinterpret_cast<const uint4*>(a.in[r]);
+  uint4 first[kStageBatch] = {};
+  if (in_vec) {
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const size_t g = c0 + tid + size_t(k) * kThreads;
+      if (g < c1) first[k] = ld_stream(s4 + g);
+    }
+  }
+
   // 2. start barrier.
   Semaphore& own = sem[r * B + b];
   uint32_t base = 0;
@@ -250,18 +268,20 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   uint16_t* bank = slots + size_t(par) * size_t(W) * stride;
 
   // 3. stage rank r's chunk b into slots[par][r].
-  const size_t G = a.n / 8u;
-  const size_t tail = a.n - 8u * G;
-  const size_t c0 = split_point(G, B, b), c1 = split_point(G, B, b + 1u);
   {
     const uint16_t* in = a.in[r];
     uint16_t* dst = bank + size_t(r) * stride;
-    if ((a.in_vec_mask >> r) & 1u) {
+    if (in_vec) {
       // Batches of kStageBatch vectors per thread: every load of a batch is
-      // in flight before the first store.
-      const uint4* s4 = reinterpret_cast<const uint4*>(in);
+      // in flight before the first store.  The first batch was loaded above.
       uint4* d4 = reinterpret_cast<uint4*>(dst);
-      for (size_t g0 = c0 + tid; g0 < c1; g0 += size_t(kStageBatch) * kThreads) {
+#pragma unroll
+      for (int k = 0; k < kStageBatch; ++k) {
+        const size_t g = c0 + tid + size_t(k) * kThreads;
+        if (g < c1) st_global(d4 + g, first[k]);
+      }
+      for (size_t g0 = c0 + tid + size_t(kStageBatch) * kThreads; g0 < c1;
+           g0 += size_t(kStageBatch) * kThreads) {
         uint4 v[kStageBatch];
 #pragma unroll
         for (int k = 0; k < kStageBatch; ++k) {
