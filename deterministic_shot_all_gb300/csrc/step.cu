@@ -8,8 +8,8 @@
 //     The per-block parity epoch (common.cuh, `PushController`, two stages)
 //     must equal (seq - 1) & 1.
 //  2. start barrier (common.cuh, `PullController::sync`, start stage,
-//     unfenced): lane 0 of warp q < W adds 1 to Semaphore sem[q][b]; warp r
-//     waits until flag - counter >= W; then the block synchronises.
+//     unfenced): lane 0 of warp q < W adds 1 to Semaphore sem[q][b]; lane 0 of
+//     warp r waits until flag - counter >= W; then the block synchronises.
 //  3. stage: rank r's chunk b -> slots[bank][r] (stands in for the RDMA write
 //     into every peer's recv[seq & 1][rank]); the last block past the copy
 //     resets the first block counter and publishes seq (arx.cu "last block
@@ -52,7 +52,11 @@
 // epochs and counters are read only by later kernels on the stream (ordered
 // by the kernel boundary) and by the host after a synchronisation, never by
 // another block of the same launch.  The pages fence there because a host
-// proxy and remote GPUs observe those words while the kernel runs.
+// proxy and remote GPUs observe those words while the kernel runs.  Semaphore
+// signals are fire-and-forget `red` adds (their old value is never needed),
+// and each block's first batch of staging loads -- reads of the caller's
+// input, which no barrier guards -- is issued before the start barrier so
+// that its DRAM latency overlaps the barrier.
 #include <atomic>
 
 #include "arx_device.cuh"
