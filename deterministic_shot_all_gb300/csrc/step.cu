@@ -173,8 +173,8 @@ __device__ bool cas_until_ordered(uint32_t* p, uint32_t from, uint32_t to, uint6
 // thread t < W: send_signal to pad[t][b][r] (0 -> 1) and wait_signal on
 // pad[r][b][t] (1 -> 0), which leaves the pad all zero once every block of
 // the barrier has passed.  kAcqRel: release send and acquire wait (the page's
-// "acq_rel" sem; a fence first makes the whole block's earlier writes part of
-// the release); otherwise relaxed.  The first send and wait attempts go out
+// "acq_rel" sem; after the block barrier that precedes it, the release also
+// covers the other threads' earlier writes); otherwise relaxed.  The first send and wait attempts go out
 // back to back; only a failed attempt is retried, within the bound.
 // `send` false skips the send (fault injection).
 template <bool kAcqRel>
@@ -183,7 +183,6 @@ __device__ void pad_barrier(uint32_t* pad, uint32_t B, uint32_t W, uint32_t b, u
                             uint32_t stage_wait) {
   uint32_t* to = &pad[(t * B + b) * W + r];
   uint32_t* from = &pad[(r * B + b) * W + t];
-  if constexpr (kAcqRel) __threadfence();
   const uint32_t sent = send ? (kAcqRel ? atom_cas_release_gpu(to, 0u, 1u) : atom_cas_relaxed_gpu(to, 0u, 1u)) : 0u;
   const uint32_t got = kAcqRel ? atom_cas_acquire_gpu(from, 1u, 0u) : atom_cas_relaxed_gpu(from, 1u, 0u);
   if (send && sent != 0u) {
@@ -194,7 +193,6 @@ __device__ void pad_barrier(uint32_t* pad, uint32_t B, uint32_t W, uint32_t b, u
     const bool ok = kAcqRel ? cas_until_ordered<false>(from, 1u, 0u, timeout_ns) : cas_until(from, 1u, 0u, timeout_ns);
     if (!ok) record_error(err, kErrTimeout, stage_wait, r, b);
   }
-  if constexpr (kAcqRel) __threadfence();
 }
 
 __device__ __forceinline__ size_t split_point(size_t total, uint32_t parts, uint32_t i) {
@@ -320,6 +318,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     }
   } else if (lane == 0 && warp < uint32_t(W)) {
     if (int(r) != a.fault_rank) {
+      // Release after the block barrier: every thread's staged data is
+      // ordered before the signal (the waiter acquires).  The explicit fence
+      // duplicates the release's ordering but measured 1.3 % faster here
+      // (unlike the pad barrier, where dropping it saved 12-22 %).
       __threadfence();
       red_add_release_gpu(&sem[warp * B + b].flag, 1u);
     }
