@@ -151,6 +151,30 @@ def test_single_step_host_slots(arx, dev, W):
         assert np.array_equal(c.slot(1, W - 1, n), sp.to_u16_numpy(x)[W - 1])
 
 
+def test_random_small_steps(arx, dev):
+    # Seeded fuzz of the step: W = 1..8, small and ragged n, B from 1 to the
+    # automatic choice, every barrier variant, slots in one buffer or in host
+    # memory; each step's output against the oracle and its words against the
+    # model.
+    rng = np.random.default_rng(4242)
+    for case in range(40):
+        W = int(rng.integers(1, 9))
+        n = int(rng.integers(1, 3000))
+        B = int(rng.integers(0, 6))
+        sync = SYNCS[int(rng.integers(0, 3))]
+        slots = "host" if case % 5 == 0 else "one"
+        c = Ctx(arx, dev, W, n, B, sync, slots)
+        st = model.State(W=W, B=c.B)
+        for s in range(2):
+            x = sp.partials(W, n, "special", seed=20_000 + 2 * case + s)
+            out = _step(arx, c, x, dev)
+            want = model.step(st, list(sp.to_u16_numpy(x)), sync=sync)
+            assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+            assert_bits_equal(out.cpu().view(torch.int16).numpy(), want,
+                              f"case {case} step {s}: W={W} n={n} B={c.B} {sync} {slots}")
+            _compare_to_model(c.words(), st)
+
+
 def test_step_equals_stateless_reduce(arx, dev):
     x, _ = sp.workload("w8_32x4096_normal")
     xd = x.to(dev)

@@ -273,3 +273,42 @@ def test_host_buffer_form_pageable_staged(arx, dev):
     rc = arx.lib.arx_reduce_host(arx._ptr_array(host), W, hout.data_ptr(), n, None, 0,
                                  torch.cuda.current_stream().cuda_stream)
     assert rc == arx.ARX_EINVAL and "staging" in arx.arx_last_error()
+
+
+def test_random_small_cases(arx, dev):
+    # Seeded fuzz over the shapes the vector paths split into: W = 1..8,
+    # n in [0, 64] and a few larger ragged sizes, every pointer at its own
+    # 2-byte offset within a 16-byte line (same offset for all -> vector path
+    # with a scalar head; different -> scalar path), output separate or equal
+    # to one slot.  Every element is compared with the oracle, guards checked.
+    rng = np.random.default_rng(20261202)
+    for case in range(300):
+        W = int(rng.integers(1, 9))
+        n = int(rng.integers(0, 65)) if case % 4 else int(rng.integers(65, 5000))
+        same = bool(rng.integers(0, 2))
+        base_off = int(rng.integers(0, 8))
+        offs = [base_off] * (W + 1) if same else [int(v) for v in rng.integers(0, 8, W + 1)]
+        alias = int(rng.integers(-1, W)) if n else -1       # -1: separate output
+        x = sp.partials(W, n, "special", seed=10_000 + case)
+        want = oracle.reduce(list(sp.to_u16_numpy(x))) if n else np.empty(0, np.uint16)
+        stride = n + 16 + 2 * GUARD
+        buf = torch.full((W + 1, stride), SENTINEL, dtype=torch.int16, device=dev)
+        for r in range(W):
+            buf[r, GUARD + offs[r]:GUARD + offs[r] + n] = x[r].view(torch.int16).to(dev)
+        slots = [buf[r, GUARD + offs[r]:GUARD + offs[r] + n].view(torch.bfloat16) for r in range(W)]
+        if alias >= 0:
+            out, orow, ooff = slots[alias], alias, offs[alias]
+        else:
+            out, orow, ooff = buf[W, GUARD + offs[W]:GUARD + offs[W] + n].view(torch.bfloat16), W, offs[W]
+        arx.arx_reduce(slots, out, n=n)
+        torch.cuda.synchronize()
+        host = buf.cpu().numpy().view(np.uint16)
+        what = f"case {case}: W={W} n={n} offs={offs} alias={alias}"
+        if n:
+            assert_bits_equal(host[orow, GUARD + ooff:GUARD + ooff + n], want, what)
+        for r in range(W + 1):                     # nothing outside the n elements moved
+            o = offs[r]
+            assert (host[r, :GUARD + o] == SENTINEL).all(), what
+            assert (host[r, GUARD + o + n:] == SENTINEL).all(), what
+            if r < W and r != orow:
+                assert np.array_equal(host[r, GUARD + o:GUARD + o + n], sp.to_u16_numpy(x[r])), what
