@@ -312,3 +312,38 @@ def test_random_small_cases(arx, dev):
             assert (host[r, GUARD + o + n:] == SENTINEL).all(), what
             if r < W and r != orow:
                 assert np.array_equal(host[r, GUARD + o:GUARD + o + n], sp.to_u16_numpy(x[r])), what
+
+
+def test_more_than_2_to_31_elements(arx, dev):
+    # W = 2 partials of 2^31 + 13 elements (4 GiB each, 12 GiB with the
+    # output): any 32-bit element or byte index in the launch would wrap.
+    # The partials are hashed from the element index on the device, and the
+    # oracle recomputes sampled outputs one by one from the same patterns:
+    # random indices plus both sides of 2^31 and 2^32 bytes and the tail.
+    W, n = 2, (1 << 31) + 13
+    free, _ = torch.cuda.mem_get_info(dev)
+    if free < 14 * 2**30:
+        pytest.skip("needs 14 GiB of free device memory")
+    x = torch.empty(W, n, dtype=torch.int16, device=dev)
+    chunk = 1 << 28
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        i = torch.arange(lo, hi, dtype=torch.int64, device=dev)
+        for r in range(W):
+            h = (i * 2654435761 + (r + 1) * 40503) & 0xFFFF
+            h = torch.where((h & 0x7F80) == 0x7F80, h & 0xBFFF, h)    # finite patterns only
+            x[r, lo:hi] = (h - ((h >= 0x8000).long() << 16)).to(torch.int16)
+    out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    arx.arx_reduce([x[0].view(torch.bfloat16), x[1].view(torch.bfloat16)], out)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(31)
+    idx = np.concatenate([rng.integers(0, n, 200_000),
+                          np.arange((1 << 31) - 64, (1 << 31) + 13), np.arange(n - 64, n),
+                          np.arange(0, 64)])
+    ti = torch.from_numpy(idx).to(dev)
+    got = out.view(torch.int16)[ti].cpu().numpy().view(np.uint16)
+    parts = [x[r][ti].cpu().numpy().view(np.uint16).copy() for r in range(W)]
+    want = oracle.reduce(parts)
+    assert_bits_equal(got, want, f"sampled outputs of a 2^31 + 13 element reduce")
+    del x, out
+    torch.cuda.empty_cache()
