@@ -175,6 +175,39 @@ def test_random_small_steps(arx, dev):
             _compare_to_model(c.words(), st)
 
 
+def test_two_contexts_step_concurrently_on_two_streams(arx, dev):
+    # Independent contexts share no state: two of them (different W and
+    # barrier variants) run 200 steps each on two streams at once -- two
+    # cooperative grids resident together, each waiting only on its own
+    # blocks -- and every output of both is checked.
+    steps = 200
+    cfg = [(8, 65536, "semaphore"), (3, 40000, "pad")]
+    ctxs, ins, outs, wants = [], [], [], []
+    for W, n, sync in cfg:
+        c = Ctx(arx, dev, W, n, 0, sync)
+        k = 4
+        xs = [sp.partials(W, n, "normal", seed=900 + 10 * W + j) for j in range(k)]
+        ins.append([x.to(dev) for x in xs])
+        wants.append([oracle.reduce(list(sp.to_u16_numpy(x))) for x in xs])
+        outs.append(torch.zeros(steps, n, dtype=torch.bfloat16, device=dev))
+        ctxs.append(c)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for t in range(steps):
+        for j, (W, n, sync) in enumerate(cfg):
+            xd = ins[j][t % 4]
+            arx.arx_step(ctxs[j].ctx, [xd[r] for r in range(W)], outs[j][t], stream=streams[j])
+    torch.cuda.synchronize()
+    for j, (W, n, sync) in enumerate(cfg):
+        st, seq, err = arx.arx_ctx_query(ctxs[j].ctx)
+        assert (st, seq, err) == (arx.ARX_OK, steps, 0), sync
+        got = outs[j].cpu().view(torch.int16).numpy().view(np.uint16)
+        for t in range(steps):
+            assert_bits_equal(got[t], wants[j][t % 4], f"context {j} step {t}")
+        w = ctxs[j].words()
+        assert not w["pad"].any() and (w["epoch"] == steps % 2).all()
+
+
 def test_step_equals_stateless_reduce(arx, dev):
     x, _ = sp.workload("w8_32x4096_normal")
     xd = x.to(dev)
