@@ -208,6 +208,24 @@ def test_two_contexts_step_concurrently_on_two_streams(arx, dev):
         assert not w["pad"].any() and (w["epoch"] == steps % 2).all()
 
 
+@pytest.mark.parametrize("sync", ["pad", "pad_fenced"])
+def test_barrier_test_pattern_pad_all_zero(arx, dev, sync):
+    # triton_barrier.py's barrier_test: the blockwise barrier on a launch of
+    # 32 blocks, then assert the signal pad is all zero.  Here 32 blocks per
+    # virtual rank run three pad barriers per step (Patterns 0, 1, 2); the pad
+    # must be all zero after every step.
+    W, n, B = 8, 32 * 8 * 64, 32
+    c = Ctx(arx, dev, W, n, B, sync)
+    assert c.B == B
+    for s in range(5):
+        x = sp.partials(W, n, "normal", seed=700 + s)
+        out = _step(arx, c, x, dev)
+        assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, s + 1, 0)
+        assert not c.words()["pad"].any(), f"pad not zero after step {s + 1}"
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                          f"step {s + 1}")
+
+
 def test_step_equals_stateless_reduce(arx, dev):
     x, _ = sp.workload("w8_32x4096_normal")
     xd = x.to(dev)
