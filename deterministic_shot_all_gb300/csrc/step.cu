@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   const uint32_t total_blocks = B * uint32_t(W);
 
   __shared__ uint32_t s_seq;
+  __shared__ uint32_t s_epoch;
   dependent_launch_prologue();
 
   // 1. seq / parity; epoch check (both words loaded back to back).
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     epoch_in = epoch[r * B + b];
     const uint32_t seq = done + 1u;
     s_seq = seq;
+    if constexpr (kPad) s_epoch = epoch_in;
     if (epoch_in != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
 
@@ -379,17 +381,34 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   }
 
   // 6. exit: zero-resetting pad barrier (Pattern 2: block barrier, then the
-  // barrier -- relaxed, or acq_rel in the fenced variant).
+  // barrier -- relaxed, or acq_rel in the fenced variant), then the epoch
+  // flip and the block-out count.  No block of this launch reads those two
+  // words (later kernels and the host see them after the kernel ends), so in
+  // the pad variants a thread outside the barrier does them concurrently with
+  // it (5.6 instead of 6.3 us per step); in the Semaphore variant the same
+  // change measured slower, so there they follow the barrier.
   __syncthreads();
-  if (tid < uint32_t(W))
-    pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
-                            kPadWait);
-  __syncthreads();
-  if (tid == 0) {
-    epoch[r * B + b] = (epoch_in + 1u) % 2u;  // PushController::exit
-    if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
-      hdr->blocks[1] = 0u;
-      st_relaxed_gpu(&hdr->seq, seq);
+  if constexpr (kPad) {
+    if (tid < uint32_t(W)) {
+      pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
+                              kPadWait);
+    } else if (tid == 32u) {
+      epoch[r * B + b] = (s_epoch + 1u) % 2u;  // PushController::exit
+      if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
+        hdr->blocks[1] = 0u;
+        st_relaxed_gpu(&hdr->seq, seq);
+      }
+    }
+  } else {
+    if (tid < uint32_t(W))
+      pad_barrier<false>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend, kPadWait);
+    __syncthreads();
+    if (tid == 0) {
+      epoch[r * B + b] = (epoch_in + 1u) % 2u;  // PushController::exit
+      if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
+        hdr->blocks[1] = 0u;
+        st_relaxed_gpu(&hdr->seq, seq);
+      }
     }
   }
 }
