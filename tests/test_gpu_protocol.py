@@ -406,6 +406,35 @@ def test_switching_sync_modes_between_steps(arx, dev):
         _compare_to_model(c.words(), st)
 
 
+def test_mixed_variants_in_one_graph(arx, dev):
+    # 999 steps captured in one graph, the barrier variant changing every
+    # step (Semaphore, pad, pad all acq_rel, ...): back-to-back dependent
+    # launches of different kernels on one context.  Every output is checked,
+    # and the final words against the model run with the same sequence.
+    W, n, steps = 5, 20000, 999
+    c = Ctx(arx, dev, W, n, 0)
+    xs = [sp.partials(W, n, "normal", seed=1500 + j) for j in range(3)]
+    xd = [x.to(dev) for x in xs]
+    wants = [oracle.reduce(list(sp.to_u16_numpy(x))) for x in xs]
+    outs = torch.zeros(steps, n, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(steps):
+            c.set_sync(SYNCS[t % 3])
+            arx.arx_step(c.ctx, [xd[t % 3][r] for r in range(W)], outs[t], stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, steps, 0)
+    got = outs.cpu().view(torch.int16).numpy().view(np.uint16)
+    for t in range(steps):
+        assert_bits_equal(got[t], wants[t % 3], f"step {t} ({SYNCS[t % 3]})")
+    st = model.State(W=W, B=c.B)
+    for t in range(steps):
+        model.step(st, list(sp.to_u16_numpy(xs[t % 3])), sync=SYNCS[t % 3])
+    _compare_to_model(c.words(), st)
+
+
 def test_unknown_sync_mode_is_rejected(arx, dev):
     c = Ctx(arx, dev, 2, 64, 1)
     with pytest.raises(arx.ArxError):
