@@ -2,10 +2,9 @@
 //
 // Some callers cannot allocate device memory when they call the step: a
 // serving engine that reserved nearly all of HBM for its own pool at start-up,
-// code running while a CUDA graph is being captured in global capture mode
-// (where cudaMalloc is refused), or a plug-in whose host framework owns every
-// allocation.  cudaMalloc/cudaFree also synchronise the device, which a
-// latency-critical caller cannot afford.  For them the step's workspace lives
+// a plug-in whose host framework owns every allocation, or a serving loop
+// whose rules forbid allocating after start-up.  cudaMalloc/cudaFree also
+// synchronise the device, which a latency-critical caller cannot afford.  For them the step's workspace lives
 // in a file-scope static device array of fixed size, which every GPU that
 // loads this library holds until the process exits.
 //

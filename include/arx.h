@@ -300,10 +300,10 @@ arx_status arx_watch_step(const arx_ctx* ctx, uint32_t target_seq, uint64_t stal
  * Allocation-free protocol step.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory at the time
  * they call: a serving engine that reserved nearly all of HBM for its own pool
- * at start-up, code running while a CUDA graph is captured in global capture
- * mode (where cudaMalloc is refused), a plug-in whose host framework owns every
- * allocation, or a latency-critical path that cannot afford the device-wide
- * synchronisation of cudaMalloc/cudaFree.
+ * at start-up, a plug-in whose host framework owns every allocation, a
+ * serving loop whose rules forbid allocating after start-up, or a
+ * latency-critical path that cannot afford the device-wide synchronisation of
+ * cudaMalloc/cudaFree.
  *
  * Same operation and result as arx_step, bit for bit, but the workspace is a
  * static device array inside this library (about 4 MiB: ARX_NOALLOC_MAX_N

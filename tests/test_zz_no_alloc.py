@@ -2,9 +2,9 @@
 static device array inside the library.
 
 That entry point serves callers that cannot allocate device memory when they
-call it (an engine that reserved nearly all HBM for its own pool, code inside
-a CUDA graph capture in global mode, a plug-in whose framework owns every
-allocation).  Here it is called through the C ABI and checked bit for bit --
+call it (an engine that reserved nearly all HBM for its own pool, a plug-in
+whose framework owns every allocation, a serving loop that forbids allocating
+after start-up).  Here it is called through the C ABI and checked bit for bit --
 the tolerance every parity test in this suite uses -- against the existing
 ``arx_step`` on two calls in a row with different inputs, so a call that
 leaked the previous call's state from the shared array would show.
