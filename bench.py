@@ -652,8 +652,22 @@ def stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R) -> dict:
             e.record(stream)
             e.synchronize()
             single.append(s.elapsed_time(e) / 1e3)
+        # The same calls through prepared plans (arguments marshalled once).
+        plans = [arx.arx_reduce_plan(slot_lists[k], outs[k], stream=stream) for k in range(R)]
+        for i in range(50):
+            plans[i % R]()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for i in range(K):
+            plans[i % R]()
+        e.record(stream)
+        torch.cuda.synchronize()
+        b2b_plan = s.elapsed_time(e) / 1e3 / K
     return {"back_to_back_us_per_call": b2b * 1e6, "calls": K,
-            "single_call_us_median": statistics.median(single) * 1e6, "single_calls": len(single)}
+            "single_call_us_median": statistics.median(single) * 1e6, "single_calls": len(single),
+            "plan_back_to_back_us_per_call": b2b_plan * 1e6}
 
 
 def hot_l2_point(torch, arx, stream, slot_lists, outs, W, n) -> dict:

@@ -210,6 +210,31 @@ def arx_reduce(slots: Sequence, out, n: int | None = None, stream=None, check: b
     return st
 
 
+class arx_reduce_plan:
+    """A prepared ``arx_reduce``: the arguments are checked and marshalled once,
+    and every call of the plan is one C call with the stored pointers, for
+    eager callers that repeat the same reduce (graph replays need no plan).
+    The plan keeps the tensors alive; their contents may change between calls,
+    their storage must not."""
+
+    def __init__(self, slots: Sequence, out, n: int | None = None, stream=None):
+        n = _numel(n, out)
+        _check_bf16(slots, n, "cuda", "slots")
+        _check_bf16([out], n, "cuda", "out")
+        self._refs = (list(slots), out)
+        self._arr = _ptr_array(slots)
+        self._W = len(slots)
+        self._out = _ptr(out)
+        self._n = n
+        self._stream = _stream(stream)
+        self._fn = lib.arx_reduce
+
+    def __call__(self) -> None:
+        st = self._fn(self._arr, self._W, self._out, self._n, self._stream)
+        if st != ARX_OK:
+            _check(st)
+
+
 def arx_reduce_host_staging_bytes(W: int, n: int) -> int:
     return int(lib.arx_reduce_host_staging_bytes(W, n))
 
@@ -354,7 +379,7 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
 
 
 __all__ = [
-    "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce",
+    "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce", "arx_reduce_plan",
     "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
     "arx_ctx_words_bytes", "arx_ctx_slots_bytes", "arx_ctx_init_split",
     "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_set_sync", "arx_ctx_reset", "arx_step", "arx_ctx_query",

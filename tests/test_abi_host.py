@@ -227,3 +227,10 @@ def test_watchdog_argument_checks(arx):
     assert w(ctypes.byref(ctx), 1, 0, 10**5, 10**9, words, None, ctypes.byref(rep)) == arx.ARX_EINVAL
     assert w(ctypes.byref(ctx), 1, 10**6, 0, 10**9, words, None, ctypes.byref(rep)) == arx.ARX_EINVAL
     assert w(ctypes.byref(ctx), 1, 10**6, 10**5, 0, words, None, None) == arx.ARX_EINVAL
+
+
+def test_plan_checks_its_arguments_once(arx):
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        arx.arx_reduce_plan([x[0], x[1]], x[0])

@@ -347,3 +347,18 @@ def test_more_than_2_to_31_elements(arx, dev):
     assert_bits_equal(got, want, f"sampled outputs of a 2^31 + 13 element reduce")
     del x, out
     torch.cuda.empty_cache()
+
+
+def test_prepared_plan_matches_and_rereads_contents(arx, dev):
+    x, _ = sp.workload("w8_32x4096_normal")
+    xd = x.to(dev)
+    out = torch.empty(x.shape[1], dtype=torch.bfloat16, device=dev)
+    plan = arx.arx_reduce_plan([xd[r] for r in range(8)], out)
+    plan()
+    torch.cuda.synchronize()
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))), "plan")
+    y = sp.partials(8, x.shape[1], "normal", seed=77)
+    xd.copy_(y.to(dev))                     # same storage, new contents
+    plan()
+    torch.cuda.synchronize()
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(y))), "plan again")
