@@ -333,6 +333,30 @@ def arx_step(ctx: arx_ctx, inputs: Sequence, out, n: int | None = None, stream=N
     return st
 
 
+class arx_step_plan:
+    """A prepared ``arx_step`` on one context (see ``arx_reduce_plan``): checked
+    and marshalled once, one C call per step.  The context's later settings
+    (sync mode, timeout, fault) apply to later calls, as it is passed by
+    reference."""
+
+    def __init__(self, ctx: arx_ctx, inputs: Sequence, out, n: int | None = None, stream=None):
+        n = _numel(n, out)
+        _check_bf16(inputs, n, "cuda", "inputs")
+        _check_bf16([out], n, "cuda", "out")
+        self._refs = (ctx, list(inputs), out)
+        self._ctx = ctypes.byref(ctx)
+        self._arr = _ptr_array(inputs)
+        self._out = _ptr(out)
+        self._n = n
+        self._stream = _stream(stream)
+        self._fn = lib.arx_step
+
+    def __call__(self) -> None:
+        st = self._fn(self._ctx, self._arr, self._out, self._n, self._stream)
+        if st != ARX_OK:
+            _check(st)
+
+
 def arx_ctx_query(ctx: arx_ctx, stream=None) -> tuple[int, int, int]:
     """Synchronise ``stream``; return (status, completed seq, device error word)."""
     seq = ctypes.c_uint32(0)
@@ -380,6 +404,7 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
 
 __all__ = [
     "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce", "arx_reduce_plan",
+    "arx_step_plan",
     "arx_reduce_host_staging_bytes", "arx_reduce_host", "arx_ctx_workspace_bytes", "arx_ctx_init",
     "arx_ctx_words_bytes", "arx_ctx_slots_bytes", "arx_ctx_init_split",
     "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_set_sync", "arx_ctx_reset", "arx_step", "arx_ctx_query",

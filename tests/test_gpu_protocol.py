@@ -226,6 +226,22 @@ def test_barrier_test_pattern_pad_all_zero(arx, dev, sync):
                           f"step {s + 1}")
 
 
+def test_step_plan(arx, dev):
+    W, n = 4, 30000
+    c = Ctx(arx, dev, W, n, 0, "pad")
+    x = sp.partials(W, n, "normal", seed=61)
+    xd = x.to(dev)
+    out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    plan = arx.arx_step_plan(c.ctx, [xd[r] for r in range(W)], out)
+    st = model.State(W=W, B=c.B)
+    for s in range(3):
+        plan()
+        want = model.step(st, list(sp.to_u16_numpy(x)), sync="pad")
+        assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"plan step {s}")
+    _compare_to_model(c.words(), st)
+
+
 def test_step_equals_stateless_reduce(arx, dev):
     x, _ = sp.workload("w8_32x4096_normal")
     xd = x.to(dev)
