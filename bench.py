@@ -515,6 +515,38 @@ def protocol_point(torch, arx, sp, dev, stream, l2, workload, steps: int = 2000)
         res["modes"][mode] = {"us_per_step": t / steps * 1e6, "status": arx.arx_status_string(st),
                               "seq": seq, "reduce_model_GBs": gbs((W + 1) * n * 2, t / steps)}
     res["us_per_step"] = res["modes"]["semaphore"]["us_per_step"]
+    del parts, outs, lists
+    torch.cuda.empty_cache()
+
+    # A bandwidth-bound step: W = 8 partials of 16 MiB (n = 2^23), each
+    # variant.  Traffic model per step: staging reads and writes W*n*2 bytes
+    # each, the reduce reads W*n*2 and writes n*2.
+    nl = 1 << 23
+    Rl = rotation_sets(W * nl * 2 * 2, l2, cap=64)
+    gen = torch.Generator(device=dev).manual_seed(4)
+    pl = (torch.randn((Rl, W, nl), generator=gen, device=dev)).to(torch.bfloat16)
+    ol = torch.empty(Rl, nl, dtype=torch.bfloat16, device=dev)
+    ll = [[pl[k, r] for r in range(W)] for k in range(Rl)]
+    large = {"n": nl, "modes": {}}
+    model_bytes = (3 * W + 1) * nl * 2
+    for mode_index, mode in enumerate(SYNC_MODES):
+        ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, nl), dtype=torch.uint8, device=dev)
+        ctx = arx.arx_ctx_init(ws, W, nl)
+        arx.arx_ctx_set_sync(ctx, mode_index)
+
+        def call(i, ctx=ctx):
+            arx.arx_step(ctx, ll[i % Rl], ol[i % Rl], stream=stream)
+
+        t = timed_graph_calls(torch, stream, call, 200, 10, chunk=200) / 200
+        st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
+        large["blocks_per_rank"] = ctx.nblocks
+        large["modes"][mode] = {"us_per_step": t * 1e6, "status": arx.arx_status_string(st),
+                                "model_GBs": gbs(model_bytes, t)}
+        del ws
+    large["traffic_model"] = "staging 2*W*n*2 B + reduce (W+1)*n*2 B per step"
+    res["large"] = large
+    del pl, ol, ll
+    torch.cuda.empty_cache()
     return res
 
 
