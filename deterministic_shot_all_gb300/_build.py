@@ -6,6 +6,10 @@ runtime linked statically (the library needs only the driver at run time).
 
 Numerics flags: no fast-math; ``-ftz=false`` keeps fp32 subnormals, which the
 bit-exact rank-order sum depends on.
+
+``--bounds-check`` (``build(bounds_check=True)``) builds the checking variant,
+``libarx_boundscheck.so``, with ``-DARX_BOUNDS_CHECK``: every data access of the
+kernels is checked against its buffer, counted and skipped when outside it.
 """
 
 from __future__ import annotations
@@ -22,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libarx.so")
+CHECK_OBJ_DIR = os.path.join(PKG, "_build_boundscheck")
+CHECK_LIB = os.path.join(PKG, "libarx_boundscheck.so")
 
 SOURCES = ["reduce.cu", "step.cu", "abi.cu", "step_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("arx_device.cuh", "arx_internal.h")] + [
@@ -48,8 +54,8 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, extra: list[str], verbose: bool) -> str:
-    obj = os.path.join(OBJ_DIR, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra: list[str], verbose: bool, obj_dir: str = OBJ_DIR) -> str:
+    obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
     path = os.path.join(CSRC, src)
     if _stale(obj, [path, *HEADERS, __file__]) or extra:
         cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", path, "-o", obj]
@@ -63,26 +69,32 @@ def _compile(src: str, extra: list[str], verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile (if stale) and return the path of ``libarx.so``."""
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          bounds_check: bool = False) -> str:
+    """Compile (if stale) and return the path of ``libarx.so`` (or of the
+    bounds-checking variant)."""
+    obj_dir, lib = (CHECK_OBJ_DIR, CHECK_LIB) if bounds_check else (OBJ_DIR, LIB)
+    os.makedirs(obj_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if bounds_check:
+        extra = extra + ["-DARX_BOUNDS_CHECK"]
     if force:
         for s in SOURCES:
-            o = os.path.join(OBJ_DIR, os.path.splitext(s)[0] + ".o")
+            o = os.path.join(obj_dir, os.path.splitext(s)[0] + ".o")
             if os.path.exists(o):
                 os.remove(o)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra, verbose or ptxas_info), SOURCES))
-    if _stale(LIB, objs) or force:
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, verbose or ptxas_info, obj_dir), SOURCES))
+    if _stale(lib, objs) or force:
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                bounds_check="--bounds-check" in sys.argv))

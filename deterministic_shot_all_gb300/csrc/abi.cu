@@ -5,6 +5,7 @@
 // and drops its 512 KB / multiple-of-8 limits.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
@@ -13,6 +14,9 @@
 
 #include "arx.h"
 #include "arx_internal.h"
+#ifdef ARX_BOUNDS_CHECK
+#include "arx_device.cuh"
+#endif
 
 namespace {
 
@@ -70,7 +74,44 @@ arx_status check_io(const void* const* in, int W, const void* out, size_t n, boo
 
 }  // namespace
 
+#ifdef ARX_BOUNDS_CHECK
+namespace {
+
+// Accesses the checking build skipped because their address fell outside
+// their buffer (one counter per device, in this library's device image).
+__device__ uint32_t g_bounds_violations;
+
+constexpr int kMaxCounterDevices = 64;
+std::atomic<uint32_t*> g_counter_address[kMaxCounterDevices];
+
+__global__ void bounds_probe_kernel(uint32_t* counter, const uint16_t* base) {
+  // One address past the end of an 8-element buffer: counted, never accessed.
+  ARX_CHECKED(base + 8, 2, base, 16, counter, atomicAdd(counter, uint32_t(base[8])));
+}
+
+}  // namespace
+#endif
+
 namespace arx {
+
+#ifdef ARX_BOUNDS_CHECK
+uint32_t* bounds_counter(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxCounterDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  uint32_t* p = g_counter_address[dev].load();
+  if (p) return p;
+  void* q = nullptr;
+  *err = cudaGetSymbolAddress(&q, g_bounds_violations);
+  if (*err != cudaSuccess || !q) return nullptr;
+  g_counter_address[dev].store(static_cast<uint32_t*>(q));
+  return static_cast<uint32_t*>(q);
+}
+#endif
 
 // For entry points defined in other translation units: the same argument
 // checks and per-thread error text as the entry points here.
@@ -115,6 +156,7 @@ arx_status arx_reduce(const void* const* slots, int W, void* out, size_t n, void
   c.n = n;
   c.W = W;
   c.out_aliases_slot = alias;
+  ARX_SET_BOUNDS_COUNTER(c);
   const cudaError_t e = arx::launch_reduce(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_reduce launch");
   return ok();
@@ -167,6 +209,7 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
     c.n = n;
     c.W = W;
     c.out_aliases_slot = alias;
+    ARX_SET_BOUNDS_COUNTER(c);
     const cudaError_t e = arx::launch_reduce(c, st);
     if (e != cudaSuccess) return fail_cuda(e, "arx_reduce_host launch");
     return ok();
@@ -192,6 +235,7 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
   c.n = n;
   c.W = W;
   c.out_aliases_slot = true;
+  ARX_SET_BOUNDS_COUNTER(c);
   cudaError_t e = arx::launch_reduce(c, st);
   if (e != cudaSuccess) return fail_cuda(e, "arx_reduce_host launch");
   e = cudaMemcpyAsync(host_out, base, n * 2, cudaMemcpyDeviceToHost, st);
@@ -425,6 +469,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.B = ctx->nblocks;
   c.fault_rank = ctx->fault_rank;
   c.sync_mode = ctx->sync_mode;
+  ARX_SET_BOUNDS_COUNTER(c);
   e = arx::launch_step(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_step launch");
   return ok();
@@ -447,6 +492,40 @@ arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, v
                 words[1], (words[1] >> 8) & 15u, (words[1] >> 12) & 15u, words[1] >> 16);
   return fail(ARX_ESTATE, "device error word 0x%08x", words[1]);
 }
+
+arx_status arx_bounds_violations(uint32_t* count, int reset) {
+#ifdef ARX_BOUNDS_CHECK
+  if (!count) return fail(ARX_EINVAL, "null count");
+  cudaError_t e = cudaSuccess;
+  uint32_t* c = arx::bounds_counter(&e);
+  if (!c) return fail_cuda(e, "bounds counter lookup");
+  e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(count, c, sizeof *count, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && reset) e = cudaMemset(c, 0, sizeof *count);
+  if (e != cudaSuccess) return fail_cuda(e, "arx_bounds_violations");
+  return ok();
+#else
+  (void)count;
+  (void)reset;
+  return fail(ARX_EINVAL, "this library was built without bounds checks");
+#endif
+}
+
+#ifdef ARX_BOUNDS_CHECK
+// Checking build only (not declared in arx.h): one deliberately out-of-range
+// address that the check counts and skips, so a test can see the counter
+// move without any out-of-range access taking place.
+arx_status arx_bounds_probe(const void* dev_buffer_16_bytes) {
+  cudaError_t e = cudaSuccess;
+  uint32_t* c = arx::bounds_counter(&e);
+  if (!c) return fail_cuda(e, "bounds counter lookup");
+  bounds_probe_kernel<<<1, 1>>>(c, static_cast<const uint16_t*>(dev_buffer_16_bytes));
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e, "arx_bounds_probe");
+  return ok();
+}
+#endif
 
 arx_status arx_watch_step(const arx_ctx* ctx, uint32_t target_seq, uint64_t stall_ns,
                           uint64_t poll_ns, uint64_t max_wait_ns, uint32_t* host_words,

@@ -142,6 +142,33 @@ __device__ __forceinline__ void st_global(uint2* p, const uint2& v) {
   asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// ---- bounds checks of the opt-in checking build -----------------------------------
+//
+// Built with ARX_BOUNDS_CHECK (`_build.py --bounds-check`, a separate
+// library), every data access of the kernels -- partials, slots, output --
+// is preceded by a check that [p, p + bytes) lies inside the buffer it
+// belongs to; a failed check adds 1 to a device counter and the access is
+// skipped, so a wrong index is counted instead of touching memory.  In the
+// normal build ARX_CHECKED(...) is exactly the access.
+#ifdef ARX_BOUNDS_CHECK
+__device__ __forceinline__ bool in_range(const void* p, size_t bytes, const void* base, size_t nbytes,
+                                         uint32_t* counter) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(base);
+  const bool ok = a >= b && a + bytes <= b + nbytes;
+  if (!ok) atomicAdd(counter, 1u);
+  return ok;
+}
+#define ARX_CHECKED(p, bytes, base, nbytes, counter, access)                     \
+  do {                                                                          \
+    if (::arx::in_range((p), (bytes), (base), (nbytes), (counter))) { access; }  \
+  } while (0)
+#else
+#define ARX_CHECKED(p, bytes, base, nbytes, counter, access) \
+  do {                                                       \
+    access;                                                  \
+  } while (0)
+#endif
+
 // ---- programmatic dependent launch ------------------------------------------------
 
 // Wait for the previous kernel of the stream (when launched as its

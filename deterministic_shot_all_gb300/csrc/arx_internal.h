@@ -23,6 +23,9 @@ struct ReduceCall {
   size_t n;
   int W;
   bool out_aliases_slot;  // out equals one slot pointer
+#ifdef ARX_BOUNDS_CHECK
+  uint32_t* bounds_counter;
+#endif
 };
 
 // Enqueues the reduce on `stream`.  Picks the vector kernel when every
@@ -41,6 +44,9 @@ struct StepCall {
   int W, B;
   int fault_rank;
   int sync_mode;  // ARX_SYNC_*
+#ifdef ARX_BOUNDS_CHECK
+  uint32_t* bounds_counter;
+#endif
 };
 
 cudaError_t launch_step(const StepCall& c, cudaStream_t stream);
@@ -51,5 +57,24 @@ int step_capacity(int W, cudaError_t* err);
 
 // SM count of the current device (cached per device ordinal).
 int current_sm_count(cudaError_t* err);
+
+#ifdef ARX_BOUNDS_CHECK
+// Device address of the checking build's violation counter on the current
+// device, or nullptr with *err set.
+uint32_t* bounds_counter(cudaError_t* err);
+
+// Sets call.bounds_counter, or returns ARX_ECUDA from the enclosing function.
+#define ARX_SET_BOUNDS_COUNTER(call)                                              \
+  do {                                                                           \
+    cudaError_t e_ = cudaSuccess;                                                \
+    (call).bounds_counter = ::arx::bounds_counter(&e_);                          \
+    if (!(call).bounds_counter)                                                  \
+      return ::arx::report(ARX_ECUDA, "bounds counter lookup: %s", cudaGetErrorString(e_)); \
+  } while (0)
+#else
+#define ARX_SET_BOUNDS_COUNTER(call) \
+  do {                               \
+  } while (0)
+#endif
 
 }  // namespace arx

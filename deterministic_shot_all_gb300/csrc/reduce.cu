@@ -47,14 +47,19 @@ struct VecArgs {
   uint16_t* out;
   size_t n;        // elements
   size_t head;     // scalar elements before the first 16-byte boundary
+#ifdef ARX_BOUNDS_CHECK
+  uint32_t* bounds_counter;
+#endif
 };
 
 template <int W>
 __device__ __forceinline__ void scalar_element(const VecArgs& a, size_t e) {
   float acc = 0.0f;
 #pragma unroll
-  for (int r = 0; r < W; ++r) acc = __fadd_rn(acc, widen16(a.slot[r][e]));
-  a.out[e] = round_bf16(acc);
+  for (int r = 0; r < W; ++r)
+    ARX_CHECKED(a.slot[r] + e, 2, a.slot[r], a.n * 2, a.bounds_counter,
+                acc = __fadd_rn(acc, widen16(a.slot[r][e])));
+  ARX_CHECKED(a.out + e, 2, a.out, a.n * 2, a.bounds_counter, a.out[e] = round_bf16(acc));
 }
 
 template <bool kAlias, typename V>
@@ -80,17 +85,22 @@ __device__ __forceinline__ void head_and_tail(const VecArgs& a) {
 
 template <int W, int U, bool kAlias>
 __device__ __forceinline__ void load_batch(uint4 (&v)[U][W], const uint4* const (&src)[W], size_t g,
-                                           size_t stride) {
+                                           size_t stride, const VecArgs& a) {
 #pragma unroll
   for (int u = 0; u < U; ++u)
 #pragma unroll
-    for (int r = 0; r < W; ++r) v[u][r] = load_group<kAlias>(src[r] + g + u * stride);
+    for (int r = 0; r < W; ++r)
+      ARX_CHECKED(src[r] + g + u * stride, 16, a.slot[r], a.n * 2, a.bounds_counter,
+                  v[u][r] = load_group<kAlias>(src[r] + g + u * stride));
 }
 
 template <int W, int U>
-__device__ __forceinline__ void store_batch(uint4* dst, const uint4 (&v)[U][W], size_t g, size_t stride) {
+__device__ __forceinline__ void store_batch(uint4* dst, const uint4 (&v)[U][W], size_t g, size_t stride,
+                                            const VecArgs& a) {
 #pragma unroll
-  for (int u = 0; u < U; ++u) st_global(dst + g + u * stride, sum_vectors<W>(v[u]));
+  for (int u = 0; u < U; ++u)
+    ARX_CHECKED(dst + g + u * stride, 16, a.out, a.n * 2, a.bounds_counter,
+                st_global(dst + g + u * stride, sum_vectors<W>(v[u])));
 }
 
 template <int W, int T, int U, bool kPipe, bool kAlias>
@@ -110,13 +120,13 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
     // Batch i+1's loads are issued before batch i is summed and stored.
     uint4 cur[U][W];
     bool have = g + size_t(U - 1) * stride < G;
-    if (have) load_batch<W, U, kAlias>(cur, src, g, stride);
+    if (have) load_batch<W, U, kAlias>(cur, src, g, stride, a);
     while (have) {
       const size_t gn = g + step;
       const bool more = gn + size_t(U - 1) * stride < G;
       uint4 nxt[U][W];
-      if (more) load_batch<W, U, kAlias>(nxt, src, gn, stride);
-      store_batch<W, U>(dst, cur, g, stride);
+      if (more) load_batch<W, U, kAlias>(nxt, src, gn, stride, a);
+      store_batch<W, U>(dst, cur, g, stride, a);
       g = gn;
       have = more;
       if (more) {
@@ -129,16 +139,17 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
   } else if constexpr (U > 1) {
     for (; g + size_t(U - 1) * stride < G; g += step) {
       uint4 v[U][W];
-      load_batch<W, U, kAlias>(v, src, g, stride);
-      store_batch<W, U>(dst, v, g, stride);
+      load_batch<W, U, kAlias>(v, src, g, stride, a);
+      store_batch<W, U>(dst, v, g, stride, a);
     }
   }
   // Remaining groups (fewer than U per thread).
   for (; g < G; g += stride) {
     uint4 v[W];
 #pragma unroll
-    for (int r = 0; r < W; ++r) v[r] = load_group<kAlias>(src[r] + g);
-    st_global(dst + g, sum_vectors<W>(v));
+    for (int r = 0; r < W; ++r)
+      ARX_CHECKED(src[r] + g, 16, a.slot[r], a.n * 2, a.bounds_counter, v[r] = load_group<kAlias>(src[r] + g));
+    ARX_CHECKED(dst + g, 16, a.out, a.n * 2, a.bounds_counter, st_global(dst + g, sum_vectors<W>(v)));
   }
 
   head_and_tail<W>(a);
@@ -158,8 +169,9 @@ __global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
   for (size_t h = size_t(blockIdx.x) * T + threadIdx.x; h < H; h += stride) {
     uint2 v[W];
 #pragma unroll
-    for (int r = 0; r < W; ++r) v[r] = load_group<kAlias>(src[r] + h);
-    st_global(dst + h, sum_halves<W>(v));
+    for (int r = 0; r < W; ++r)
+      ARX_CHECKED(src[r] + h, 8, a.slot[r], a.n * 2, a.bounds_counter, v[r] = load_group<kAlias>(src[r] + h));
+    ARX_CHECKED(dst + h, 8, a.out, a.n * 2, a.bounds_counter, st_global(dst + h, sum_halves<W>(v)));
   }
   head_and_tail<W>(a);
 }
@@ -260,6 +272,9 @@ cudaError_t launch_w(const ReduceCall& c, cudaStream_t stream) {
   for (int r = 0; r < W; ++r) a.slot[r] = c.slot[r];
   a.out = c.out;
   a.n = c.n;
+#ifdef ARX_BOUNDS_CHECK
+  a.bounds_counter = c.bounds_counter;
+#endif
 
   cudaError_t err = cudaSuccess;
   int dev = 0;

@@ -106,6 +106,9 @@ struct StepArgs {
   int fault_rank;
   uint32_t in_vec_mask;  // bit r: input r is 16-byte aligned
   int out_vec;           // out is 16-byte aligned
+#ifdef ARX_BOUNDS_CHECK
+  uint32_t* bounds_counter;
+#endif
 };
 
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code, uint32_t stage,
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 #pragma unroll
     for (int k = 0; k < kStageBatch; ++k) {
       const size_t g = c0 + tid + size_t(k) * kThreads;
-      if (g < c1) first[k] = ld_stream(s4 + g);
+      if (g < c1) ARX_CHECKED(s4 + g, 16, a.in[r], a.n * 2, a.bounds_counter, first[k] = ld_stream(s4 + g));
     }
   }
 
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 #pragma unroll
       for (int k = 0; k < kStageBatch; ++k) {
         const size_t g = c0 + tid + size_t(k) * kThreads;
-        if (g < c1) st_global(d4 + g, first[k]);
+        if (g < c1) ARX_CHECKED(d4 + g, 16, a.slots, size_t(4) * W * a.slot_stride, a.bounds_counter, st_global(d4 + g, first[k]));
       }
       for (size_t g0 = c0 + tid + size_t(kStageBatch) * kThreads; g0 < c1;
            g0 += size_t(kStageBatch) * kThreads) {
@@ -290,18 +293,21 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 #pragma unroll
         for (int k = 0; k < kStageBatch; ++k) {
           const size_t g = g0 + size_t(k) * kThreads;
-          if (g < c1) v[k] = ld_stream(s4 + g);
+          if (g < c1) ARX_CHECKED(s4 + g, 16, a.in[r], a.n * 2, a.bounds_counter, v[k] = ld_stream(s4 + g));
         }
 #pragma unroll
         for (int k = 0; k < kStageBatch; ++k) {
           const size_t g = g0 + size_t(k) * kThreads;
-          if (g < c1) st_global(d4 + g, v[k]);
+          if (g < c1) ARX_CHECKED(d4 + g, 16, a.slots, size_t(4) * W * a.slot_stride, a.bounds_counter, st_global(d4 + g, v[k]));
         }
       }
     } else {
-      for (size_t e = 8u * c0 + tid; e < 8u * c1; e += kThreads) dst[e] = in[e];
+      for (size_t e = 8u * c0 + tid; e < 8u * c1; e += kThreads)
+        ARX_CHECKED(in + e, 2, a.in[r], a.n * 2, a.bounds_counter, ARX_CHECKED(dst + e, 2, a.slots, size_t(4) * W * a.slot_stride, a.bounds_counter, dst[e] = in[e]));
     }
-    if (b == B - 1u && tid < tail) dst[8u * G + tid] = in[8u * G + tid];
+    if (b == B - 1u && tid < tail)
+      ARX_CHECKED(in + 8u * G + tid, 2, a.in[r], a.n * 2, a.bounds_counter,
+                  ARX_CHECKED(dst + 8u * G + tid, 2, a.slots, size_t(4) * W * a.slot_stride, a.bounds_counter, dst[8u * G + tid] = in[8u * G + tid]));
   }
   // 4. end barrier, fenced: every thread's staging precedes the release.
   __syncthreads();
@@ -355,28 +361,33 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     for (size_t g = s0 + tid; g < s1; g += kThreads) {
       uint4 v[W];
 #pragma unroll
-      for (int q = 0; q < W; ++q) v[q] = ld_cg(src[q] + g);
+      for (int q = 0; q < W; ++q) ARX_CHECKED(src[q] + g, 16, a.slots, size_t(4) * W * a.slot_stride, a.bounds_counter, v[q] = ld_cg(src[q] + g));
       const uint4 o = sum_vectors<W>(v);
       if (a.out_vec) {
-        st_global(reinterpret_cast<uint4*>(a.out) + g, o);
+        ARX_CHECKED(reinterpret_cast<uint4*>(a.out) + g, 16, a.out, a.n * 2, a.bounds_counter,
+                    st_global(reinterpret_cast<uint4*>(a.out) + g, o));
       } else {
         uint16_t* d = a.out + 8u * g;
-        d[0] = uint16_t(o.x & 0xFFFFu);
-        d[1] = uint16_t(o.x >> 16);
-        d[2] = uint16_t(o.y & 0xFFFFu);
-        d[3] = uint16_t(o.y >> 16);
-        d[4] = uint16_t(o.z & 0xFFFFu);
-        d[5] = uint16_t(o.z >> 16);
-        d[6] = uint16_t(o.w & 0xFFFFu);
-        d[7] = uint16_t(o.w >> 16);
+        ARX_CHECKED(d, 16, a.out, a.n * 2, a.bounds_counter, {
+          d[0] = uint16_t(o.x & 0xFFFFu);
+          d[1] = uint16_t(o.x >> 16);
+          d[2] = uint16_t(o.y & 0xFFFFu);
+          d[3] = uint16_t(o.y >> 16);
+          d[4] = uint16_t(o.z & 0xFFFFu);
+          d[5] = uint16_t(o.z >> 16);
+          d[6] = uint16_t(o.w & 0xFFFFu);
+          d[7] = uint16_t(o.w >> 16);
+        });
       }
     }
     if (b == B - 1u && r == uint32_t(W) - 1u && tid < tail) {
       const size_t e = 8u * G + tid;
       float acc = 0.0f;
 #pragma unroll
-      for (int q = 0; q < W; ++q) acc = __fadd_rn(acc, widen16(ld_cg16(bank + size_t(q) * stride + e)));
-      a.out[e] = round_bf16(acc);
+      for (int q = 0; q < W; ++q)
+        ARX_CHECKED(bank + size_t(q) * stride + e, 2, a.slots, size_t(4) * W * a.slot_stride, a.bounds_counter,
+                    acc = __fadd_rn(acc, widen16(ld_cg16(bank + size_t(q) * stride + e))));
+      ARX_CHECKED(a.out + e, 2, a.out, a.n * 2, a.bounds_counter, a.out[e] = round_bf16(acc));
     }
   }
 
@@ -450,6 +461,9 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   a.off_pad = c.off_pad;
   a.slots = c.slots;
   a.slot_stride = c.slot_stride;
+#ifdef ARX_BOUNDS_CHECK
+  a.bounds_counter = c.bounds_counter;
+#endif
   a.timeout_ns = c.timeout_ns;
   a.B = c.B;
   a.fault_rank = c.fault_rank;

@@ -122,6 +122,7 @@ extern "C" arx_status arx_step_noalloc(const void* const* inputs, int W, void* o
   c.W = W;
   c.B = int(B);
   c.fault_rank = -1;
+  ARX_SET_BOUNDS_COUNTER(c);
   e = arx::launch_step(c, s);
   if (e != cudaSuccess) return arx::report(ARX_ECUDA, "arx_step_noalloc: launch: %s", cudaGetErrorString(e));
   if (dev_status) {

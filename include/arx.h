@@ -263,6 +263,18 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
 arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Bounds checks.  The library can be built a second way, with every data
+ * access of its kernels (partials, slots, output) checked against the buffer
+ * it belongs to (`python deterministic_shot_all_gb300/_build.py
+ * --bounds-check`, which writes libarx_boundscheck.so).  A failed check is
+ * counted and the access skipped.  In that build this call reads the count
+ * of skipped accesses since the last reset into *count (and zeroes it if
+ * reset != 0); it synchronises the device.  The normal build returns
+ * ARX_EINVAL: it has no checks.
+ * ------------------------------------------------------------------------- */
+arx_status arx_bounds_violations(uint32_t* count, int reset);
+
+/* ---------------------------------------------------------------------------
  * Host-side watchdog of the protocol step (arx.cu's proxy watchdog: a step
  * published but not done for too long is reported once as a stall).
  *

@@ -1,0 +1,133 @@
+"""Random cases through the bounds-checking build of the library.
+
+``libarx_boundscheck.so`` is the same library built with ``ARX_BOUNDS_CHECK``:
+every data access of the reduce and step kernels (partials, slots, output)
+is first checked against the buffer it belongs to; a failed check is counted
+and the access skipped.  With compute-sanitizer unavailable, this stands in
+for an out-of-bounds detector: random shapes, offsets, aliasing, block counts
+and barrier variants must give the oracle's bits with a counter of zero.  A
+probe shows the counter moves on an out-of-range address (which it never
+accesses).
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_partials as sp
+from test_gpu_reduce import assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def checked(arx):
+    import importlib.util
+    import os
+    from conftest import ROOT
+    spec = importlib.util.spec_from_file_location(
+        "arx_build_check", os.path.join(ROOT, "deterministic_shot_all_gb300", "_build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    L = ctypes.CDLL(b.build(bounds_check=True))
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    ptrs = ctypes.POINTER(ctypes.c_void_p)
+    ctxp = ctypes.POINTER(arx.arx_ctx)
+    for name, args, res in (
+            ("arx_reduce", [ptrs, i32, vp, sz, vp], i32),
+            ("arx_ctx_workspace_bytes", [i32, sz, i32], sz),
+            ("arx_ctx_init", [ctxp, vp, sz, i32, sz, i32], i32),
+            ("arx_ctx_set_sync", [ctxp, i32], i32),
+            ("arx_step", [ctxp, ptrs, vp, sz, vp], i32),
+            ("arx_bounds_violations", [ctypes.POINTER(ctypes.c_uint32), i32], i32),
+            ("arx_bounds_probe", [vp], i32),
+            ("arx_last_error", [], ctypes.c_char_p)):
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
+def _violations(L, reset=True) -> int:
+    c = ctypes.c_uint32(0)
+    assert L.arx_bounds_violations(ctypes.byref(c), 1 if reset else 0) == 0, L.arx_last_error()
+    return c.value
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def test_release_build_has_no_checks(arx):
+    c = ctypes.c_uint32(0)
+    assert arx.lib.arx_bounds_violations(ctypes.byref(c), 0) == arx.ARX_EINVAL
+
+
+def test_counter_counts_an_out_of_range_address(checked):
+    dev = torch.device("cuda:0")
+    _violations(checked)
+    buf = torch.zeros(16, dtype=torch.uint8, device=dev)
+    assert checked.arx_bounds_probe(buf.data_ptr()) == 0
+    assert _violations(checked) == 1
+    assert _violations(checked) == 0
+
+
+def test_random_reduces_stay_in_bounds(checked):
+    dev = torch.device("cuda:0")
+    _violations(checked)
+    rng = np.random.default_rng(5150)
+    sizes = [(1 << 22) - 3, (1 << 22) + 9, (1 << 23) + 5]
+    for case in range(120):
+        W = int(rng.integers(1, 9))
+        n = sizes[case % 3] if case % 10 == 0 else int(rng.integers(0, 5000))
+        same = bool(rng.integers(0, 2))
+        offs = [int(rng.integers(0, 8))] * (W + 1) if same else [int(v) for v in rng.integers(0, 8, W + 1)]
+        alias = int(rng.integers(-1, W)) if n else -1
+        x = sp.partials(W, n, "special" if n < 10000 else "normal", seed=30_000 + case)
+        buf = torch.zeros(W + 1, n + 16, dtype=torch.int16, device=dev)
+        for r in range(W):
+            buf[r, offs[r]:offs[r] + n] = x[r].view(torch.int16).to(dev)
+        slots = [buf[r, offs[r]:offs[r] + n] for r in range(W)]
+        out = slots[alias] if alias >= 0 else buf[W, offs[W]:offs[W] + n]
+        arr = (ctypes.c_void_p * W)(*[t.data_ptr() for t in slots])
+        assert checked.arx_reduce(arr, W, out.data_ptr(), n, _stream()) == 0, checked.arx_last_error()
+        torch.cuda.synchronize()
+        if n:
+            want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+            assert_bits_equal(out.cpu().numpy().view(np.uint16), want,
+                              f"case {case}: W={W} n={n} offs={offs} alias={alias}")
+    assert _violations(checked) == 0
+
+
+def test_random_steps_stay_in_bounds(checked, arx):
+    dev = torch.device("cuda:0")
+    _violations(checked)
+    rng = np.random.default_rng(6160)
+    for case in range(30):
+        W = int(rng.integers(1, 9))
+        n = int(rng.integers(1, 40000)) if case % 6 else 1 << 20
+        B = int(rng.integers(0, 8))
+        mode = int(rng.integers(0, 3))
+        in_off, out_off = int(rng.integers(0, 8)), int(rng.integers(0, 8))
+        ws = torch.zeros(checked.arx_ctx_workspace_bytes(W, n, B), dtype=torch.uint8, device=dev)
+        ctx = arx.arx_ctx()
+        assert checked.arx_ctx_init(ctypes.byref(ctx), ws.data_ptr(), ws.numel(), W, n, B) == 0
+        assert checked.arx_ctx_set_sync(ctypes.byref(ctx), mode) == 0
+        for s in range(2):
+            x = sp.partials(W, n, "normal", seed=40_000 + 2 * case + s)
+            buf = torch.zeros(W, n + 16, dtype=torch.int16, device=dev)
+            buf[:, in_off:in_off + n] = x.view(torch.int16).to(dev)
+            ins = (ctypes.c_void_p * W)(*[buf[r, in_off:in_off + n].data_ptr() for r in range(W)])
+            ob = torch.zeros(n + 16, dtype=torch.int16, device=dev)
+            out = ob[out_off:out_off + n]
+            assert checked.arx_step(ctypes.byref(ctx), ins, out.data_ptr(), n, _stream()) == 0
+            torch.cuda.synchronize()
+            want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+            assert_bits_equal(out.cpu().numpy().view(np.uint16), want,
+                              f"case {case} step {s}: W={W} n={n} B={ctx.nblocks} mode={mode}")
+        words = ws[:8].cpu().numpy().view(np.uint32)
+        assert words[0] == 2 and words[1] == 0, f"case {case}: seq {words[0]} err {words[1]:#x}"
+    assert _violations(checked) == 0
