@@ -73,3 +73,29 @@ def test_reference_arm_prints_one_line(steps, capsys):
     rec = json.loads(line[0])
     assert rec["impl"] == "reference" and rec["steps"] == steps and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _reference_worker(rank, world, results):
+    import contextlib
+    import io
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"])
+    results[rank] = buf.getvalue()
+
+
+def test_reference_arm_prints_on_rank_0_only():
+    world = 2
+    mgr = tmp.get_context("spawn").Manager()
+    results = mgr.dict()
+    tmp.start_processes(_reference_worker, args=(world, results), nprocs=world, join=True,
+                        start_method="spawn")
+    import json
+    lines = results[0].strip().splitlines()
+    assert len(lines) == 1 and json.loads(lines[0])["impl"] == "reference"
+    assert json.loads(lines[0])["n_gpus"] == world
+    assert results[1] == ""
