@@ -156,6 +156,7 @@ arx_status arx_reduce(const void* const* slots, int W, void* out, size_t n, void
   c.n = n;
   c.W = W;
   c.out_aliases_slot = alias;
+  c.prefetch_l2 = true;
   ARX_SET_BOUNDS_COUNTER(c);
   const cudaError_t e = arx::launch_reduce(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_reduce launch");

@@ -169,6 +169,12 @@ __device__ __forceinline__ bool in_range(const void* p, size_t bytes, const void
   } while (0)
 #endif
 
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple
+// of 16).  A hint only: no data is returned and nothing is made visible.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 // ---- programmatic dependent launch ------------------------------------------------
 
 // Wait for the previous kernel of the stream (when launched as its

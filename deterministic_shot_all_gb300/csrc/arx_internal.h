@@ -23,6 +23,7 @@ struct ReduceCall {
   size_t n;
   int W;
   bool out_aliases_slot;  // out equals one slot pointer
+  bool prefetch_l2;       // buffers are device memory: the kernel may prefetch them into L2
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif

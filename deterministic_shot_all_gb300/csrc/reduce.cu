@@ -23,7 +23,13 @@
 //  * programmatic dependent launch: the kernel waits on its stream
 //    predecessor (griddepcontrol.wait) before touching memory and lets its
 //    successor start launching at once, which hides most of the launch gap
-//    between back-to-back calls.
+//    between back-to-back calls;
+//  * before that wait, one thread per block issues bulk L2 prefetches of the
+//    block's first chunk of every slot (device buffers only), so the next
+//    call's DRAM latency overlaps the current call -- a prefetch consumes no
+//    data, so a predecessor that writes those partials stays correct (the
+//    loads come after the wait and read through L2).  W = 8 [32, 4096]:
+//    1.60 -> 1.42 us per call; W = 2 at 2^23 elements: 8.76 -> 7.66 us.
 // The launch policy (threads, U, kPipe per W and size) comes from a measured
 // sweep of these shapes on GB300.
 #include <atomic>
@@ -47,6 +53,7 @@ struct VecArgs {
   uint16_t* out;
   size_t n;        // elements
   size_t head;     // scalar elements before the first 16-byte boundary
+  int prefetch_l2; // device-memory buffers: warm L2 before the dependency wait
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif
@@ -105,6 +112,20 @@ __device__ __forceinline__ void store_batch(uint4* dst, const uint4 (&v)[U][W], 
 
 template <int W, int T, int U, bool kPipe, bool kAlias>
 __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
+  // As in reduce_half_kernel: the block's first batch (U chunks of T groups
+  // per slot) is prefetched into L2 before the dependency wait.
+  if (a.prefetch_l2 && threadIdx.x == 0) {
+    const size_t stride0 = size_t(gridDim.x) * T;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const size_t first = size_t(blockIdx.x) * T + size_t(u) * stride0;
+      if (first < a.groups) {
+        const size_t cnt = a.groups - first < size_t(T) ? a.groups - first : size_t(T);
+#pragma unroll
+        for (int r = 0; r < W; ++r) prefetch_l2_bulk(a.body_src[r] + 8 * first, uint32_t(cnt * 16));
+      }
+    }
+  }
   dependent_launch_prologue();
   const uint4* src[W];
 #pragma unroll
@@ -159,6 +180,21 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
 // one vector per slot per thread per iteration.
 template <int W, int T, bool kAlias>
 __global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
+  // Before waiting for the previous kernel of the stream: ask L2 for this
+  // block's first chunk of every slot, so its DRAM latency overlaps that
+  // kernel's tail.  Only a prefetch (no data consumed), so it is safe even
+  // when the previous kernel writes these partials: the loads below come
+  // after the wait and see its writes through L2.
+  if (a.prefetch_l2 && threadIdx.x == 0) {
+    const size_t first = size_t(blockIdx.x) * T;  // first 8-byte vector of the block
+    const size_t H = 2 * a.groups;
+    if (first < H) {
+      const size_t cnt = (H - first < size_t(T) ? H - first : size_t(T)) & ~size_t(1);
+      if (cnt)
+#pragma unroll
+        for (int r = 0; r < W; ++r) prefetch_l2_bulk(a.body_src[r] + 4 * first, uint32_t(cnt * 8));
+    }
+  }
   dependent_launch_prologue();
   const uint2* src[W];
 #pragma unroll
@@ -272,6 +308,7 @@ cudaError_t launch_w(const ReduceCall& c, cudaStream_t stream) {
   for (int r = 0; r < W; ++r) a.slot[r] = c.slot[r];
   a.out = c.out;
   a.n = c.n;
+  a.prefetch_l2 = c.prefetch_l2 ? 1 : 0;
 #ifdef ARX_BOUNDS_CHECK
   a.bounds_counter = c.bounds_counter;
 #endif

@@ -67,9 +67,12 @@ const char* arx_last_error(void);
  * for 0 <= i < n, every add in fp32 round-to-nearest-even, subnormals kept
  * (arx.cu, `arx_kernel`, reduce loop).
  *
- *   slots   HOST array of W device pointers, each to n bf16 elements.  The
- *           array itself is read during the call only (it is copied into the
- *           kernel's parameters).  Slots may repeat or overlap each other.
+ *   slots   HOST array of W device pointers (device memory), each to n
+ *           bf16 elements.  The array itself is read during the call only (it
+ *           is copied into the kernel's parameters).  Slots may repeat or
+ *           overlap each other.  The kernel may prefetch them into L2 before
+ *           the previous kernel on the stream has finished (a hint: the data
+ *           it sums are read after that kernel's writes).
  *   W       1 <= W <= ARX_MAX_W.  (The page requires W >= 2; W = 1 is the
  *           identity, except that -0 becomes +0.)
  *   out     device pointer to n bf16 elements.  It may be exactly equal to
