@@ -275,6 +275,9 @@ def timed_graph_calls(torch, stream, fn, steps: int, warmup: int, chunk: int = G
                       sampler: ClockSampler | None = None) -> float:
     """Seconds for exactly ``steps`` calls of fn(i), launched from CUDA graphs on ``stream``."""
     chunk = max(1, min(chunk, steps))
+    # Inputs, outputs and zero-filled workspaces were made on torch's default
+    # stream; `stream` is a non-blocking stream, so order them before its calls.
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(max(1, min(warmup, 8))):   # eager warm-up (launch caches, lazy init)
             fn(i)
@@ -345,6 +348,7 @@ def run_native(args) -> None:
     if rank == 0 and not args.no_check:
         import oracle
         want = oracle.reduce(list(sp.to_u16_numpy(x)))
+        torch.cuda.synchronize()        # the copies above ran on the default stream
         with torch.cuda.stream(stream):
             call(0)
         torch.cuda.synchronize()
@@ -541,7 +545,7 @@ def protocol_point(torch, arx, sp, dev, stream, l2, workload, steps: int = 2000)
         st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
         large["blocks_per_rank"] = ctx.nblocks
         large["modes"][mode] = {"us_per_step": t * 1e6, "status": arx.arx_status_string(st),
-                                "model_GBs": gbs(model_bytes, t)}
+                                "seq": seq, "dev_err": err, "model_GBs": gbs(model_bytes, t)}
         del ws
     large["traffic_model"] = "staging 2*W*n*2 B + reduce (W+1)*n*2 B per step"
     res["large"] = large

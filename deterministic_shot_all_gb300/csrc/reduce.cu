@@ -122,7 +122,9 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
       if (first < a.groups) {
         const size_t cnt = a.groups - first < size_t(T) ? a.groups - first : size_t(T);
 #pragma unroll
-        for (int r = 0; r < W; ++r) prefetch_l2_bulk(a.body_src[r] + 8 * first, uint32_t(cnt * 16));
+        for (int r = 0; r < W; ++r)
+          ARX_CHECKED(a.body_src[r] + 8 * first, cnt * 16, a.slot[r], a.n * 2, a.bounds_counter,
+                      prefetch_l2_bulk(a.body_src[r] + 8 * first, uint32_t(cnt * 16)));
       }
     }
   }
@@ -192,7 +194,9 @@ __global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
       const size_t cnt = (H - first < size_t(T) ? H - first : size_t(T)) & ~size_t(1);
       if (cnt)
 #pragma unroll
-        for (int r = 0; r < W; ++r) prefetch_l2_bulk(a.body_src[r] + 4 * first, uint32_t(cnt * 8));
+        for (int r = 0; r < W; ++r)
+          ARX_CHECKED(a.body_src[r] + 4 * first, cnt * 8, a.slot[r], a.n * 2, a.bounds_counter,
+                      prefetch_l2_bulk(a.body_src[r] + 4 * first, uint32_t(cnt * 8)));
     }
   }
   dependent_launch_prologue();
