@@ -410,7 +410,7 @@ def run_native(args) -> None:
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic,
-                     "kernel": reduce_kernel_name(W, n, alias), "algorithmic_bytes_per_launch": bytes_call},
+                     "kernel": reduce_kernel_name(W, n, alias, props.multi_processor_count), "algorithmic_bytes_per_launch": bytes_call},
         "cpu_baseline": cpu,
         "cpu_baseline_1thread": cpu1,
         "gpu_launches": args.steps,
@@ -423,11 +423,19 @@ def run_native(args) -> None:
 HALF_MAX_ELEMS = 1 << 22   # the library's switch from 8-byte to 16-byte vectors
 
 
-def reduce_kernel_name(W: int, n: int, alias: bool) -> str:
-    """The kernel the library launches for this shape (its launch policy, restated)."""
+def reduce_kernel_name(W: int, n: int, alias: bool, sms: int = 152) -> str:
+    """The kernel the library launches for this shape (its launch policy, restated).
+
+    Exact for the one-vector 8-byte form (W >= 5, or one pass of a grid of
+    sms x 8 blocks of 256 threads covers the n / 4 vectors, as at the
+    decode-sized workloads); larger W <= 4 messages up to 2^22 elements take
+    a batched 8-byte form or the 16-byte one by the library's one-pass rule.
+    """
     a = "true" if alias else "false"
     if n <= HALF_MAX_ELEMS:
-        return f"reduce_half_kernel<{W}, 256, {a}>"
+        if W >= 5 or -(-(n // 4) // 256) <= sms * 8:
+            return f"reduce_half_kernel<{W}, 256, 1, {a}>"
+        return f"reduce_half_kernel<{W}, 256, U, {a}> (batched) or reduce_vec_kernel (one-pass rule)"
     if W <= 2:
         return f"reduce_vec_kernel<{W}, 128, 2, pipelined, {a}>"
     if W <= 4:

@@ -179,24 +179,33 @@ __global__ void __launch_bounds__(T) reduce_vec_kernel(const VecArgs a) {
 }
 
 // 8-byte form: the 16-byte-aligned body as 2 * groups vectors of 4 elements,
-// one vector per slot per thread per iteration.
-template <int W, int T, bool kAlias>
-__global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
+// U vectors per slot per thread per iteration (U strides apart), all W * U
+// loads issued before the first add.  U = 1 unless the body needs more than
+// one pass of the grid and W <= 4; then U = 8 / W (rounded) so each thread
+// keeps about 8 loads in flight (Little's law against HBM latency), used
+// while one pass of that grid still covers the body; W = 2, 3 have a second
+// tier twice as deep.
+template <int W, int T, int U, bool kAlias>
+__device__ __forceinline__ void reduce_half_body(const VecArgs& a) {
   // Before waiting for the previous kernel of the stream: ask L2 for this
-  // block's first chunk of every slot, so its DRAM latency overlaps that
-  // kernel's tail.  Only a prefetch (no data consumed), so it is safe even
-  // when the previous kernel writes these partials: the loads below come
-  // after the wait and see its writes through L2.
+  // block's first chunk (U chunks when U > 1) of every slot, so its DRAM
+  // latency overlaps that kernel's tail.  Only a prefetch (no data consumed),
+  // so it is safe even when the previous kernel writes these partials: the
+  // loads below come after the wait and see its writes through L2.
+  const size_t H = 2 * a.groups;
+  const size_t stride = size_t(gridDim.x) * T;
   if (a.prefetch_l2 && threadIdx.x == 0) {
-    const size_t first = size_t(blockIdx.x) * T;  // first 8-byte vector of the block
-    const size_t H = 2 * a.groups;
-    if (first < H) {
-      const size_t cnt = (H - first < size_t(T) ? H - first : size_t(T)) & ~size_t(1);
-      if (cnt)
 #pragma unroll
-        for (int r = 0; r < W; ++r)
-          ARX_CHECKED(a.body_src[r] + 4 * first, cnt * 8, a.slot[r], a.n * 2, a.bounds_counter,
-                      prefetch_l2_bulk(a.body_src[r] + 4 * first, uint32_t(cnt * 8)));
+    for (int u = 0; u < U; ++u) {
+      const size_t first = size_t(blockIdx.x) * T + size_t(u) * stride;  // even: T is
+      if (first < H) {
+        const size_t cnt = (H - first < size_t(T) ? H - first : size_t(T)) & ~size_t(1);
+        if (cnt)
+#pragma unroll
+          for (int r = 0; r < W; ++r)
+            ARX_CHECKED(a.body_src[r] + 4 * first, cnt * 8, a.slot[r], a.n * 2, a.bounds_counter,
+                        prefetch_l2_bulk(a.body_src[r] + 4 * first, uint32_t(cnt * 8)));
+      }
     }
   }
   dependent_launch_prologue();
@@ -204,16 +213,37 @@ __global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
 #pragma unroll
   for (int r = 0; r < W; ++r) src[r] = reinterpret_cast<const uint2*>(a.body_src[r]);
   uint2* dst = reinterpret_cast<uint2*>(a.body_dst);
-  const size_t H = 2 * a.groups;
-  const size_t stride = size_t(gridDim.x) * T;
-  for (size_t h = size_t(blockIdx.x) * T + threadIdx.x; h < H; h += stride) {
-    uint2 v[W];
+  for (size_t h = size_t(blockIdx.x) * T + threadIdx.x; h < H; h += size_t(U) * stride) {
+    uint2 v[U][W];
 #pragma unroll
-    for (int r = 0; r < W; ++r)
-      ARX_CHECKED(src[r] + h, 8, a.slot[r], a.n * 2, a.bounds_counter, v[r] = load_group<kAlias>(src[r] + h));
-    ARX_CHECKED(dst + h, 8, a.out, a.n * 2, a.bounds_counter, st_global(dst + h, sum_halves<W>(v)));
+    for (int u = 0; u < U; ++u) {
+      const size_t hu = h + size_t(u) * stride;
+      if (hu < H)
+#pragma unroll
+        for (int r = 0; r < W; ++r)
+          ARX_CHECKED(src[r] + hu, 8, a.slot[r], a.n * 2, a.bounds_counter, v[u][r] = load_group<kAlias>(src[r] + hu));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const size_t hu = h + size_t(u) * stride;
+      if (hu < H) ARX_CHECKED(dst + hu, 8, a.out, a.n * 2, a.bounds_counter, st_global(dst + hu, sum_halves<W>(v[u])));
+    }
   }
   head_and_tail<W>(a);
+}
+
+template <int W, int T, int U, bool kAlias>
+__global__ void __launch_bounds__(T) reduce_half_kernel(const VecArgs a) {
+  reduce_half_body<W, T, U, kAlias>(a);
+}
+
+// The 16-load form (W * U = 16) under a register bound that keeps four
+// blocks resident per SM (64 registers; left to itself it takes 69 and fits
+// three).  A separate entry point because a minimum-blocks bound on the
+// other instances changes their register allocation too.
+template <int W, int T, int U, bool kAlias>
+__global__ void __launch_bounds__(T, 4) reduce_half_deep_kernel(const VecArgs a) {
+  reduce_half_body<W, T, U, kAlias>(a);
 }
 
 // Pointers with different addresses mod 16: one element per thread per step.
@@ -272,23 +302,54 @@ cudaError_t launch_vec(const VecArgs& a, int dev, int sms, cudaStream_t stream) 
   return launch_dependent(k, blocks, T, stream, a);
 }
 
-template <int W, int T, bool kAlias>
-cudaError_t launch_half(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
+// 8-byte vectors per slot per thread per iteration of the batched 8-byte
+// form: about 8 loads in flight per thread at every W.
+template <int W>
+constexpr int kHalfU = W >= 5 ? 1 : W >= 3 ? 2 : W == 2 ? 4 : 8;
+// A second batched tier, twice as deep, where its one-pass reach is larger
+// despite the lower residency its registers allow (W = 2, 3); 0 = none.
+template <int W>
+constexpr int kHalfU2 = W == 2 || W == 3 ? 2 * kHalfU<W> : 0;
+
+// Launches the 8-byte form with U vectors per slot per thread if one pass
+// of its grid (SMs x resident blocks x T threads x U) covers the body --
+// with 1/16 slack: a second pass for a few threads costs little, one for a
+// fifth of them 10-30 % -- or always when `force`.  Sets *taken; returns
+// the launch status.
+template <int W, int T, int U, bool kAlias>
+cudaError_t launch_half(const VecArgs& a, int dev, int sms, bool force, bool* taken,
+                        cudaStream_t stream) {
   static std::atomic<int> cache[kMaxDevices];
   cudaError_t err = cudaSuccess;
-  auto k = reduce_half_kernel<W, T, kAlias>;
+  *taken = false;
+  void (*k)(VecArgs) = nullptr;
+  if constexpr (W * U >= 16) {
+    k = reduce_half_deep_kernel<W, T, U, kAlias>;
+  } else {
+    k = reduce_half_kernel<W, T, U, kAlias>;
+  }
   const int per_sm = blocks_per_sm(k, T, dev, cache, &err);
   if (per_sm < 1) return err;
   size_t blocks = (2 * a.groups + T - 1) / T;
   const size_t cap = size_t(sms) * size_t(per_sm);
+  if (!force && blocks * 16u > cap * size_t(U) * 17u) return cudaSuccess;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  *taken = true;
   return launch_dependent(k, blocks, T, stream, a);
 }
 
 // Measured policy (launch-shape sweeps of W = 2, 4, 8 from 2^15 to 2^27
-// elements per partial on GB300, CUDA-graph replays, inputs beyond L2):
-//  n <= 2^22: 8-byte vectors, 256 threads, every W;
+// elements per partial, and a sweep of W = 1-4 from 2^20.5 to 2^22 in
+// quarter powers, on GB300, CUDA-graph replays, inputs beyond L2):
+//  n <= 2^22: the 8-byte form.  W >= 5: one vector per slot per thread.
+//             W <= 4: one vector while one pass of the grid covers the
+//             body, else kHalfU<W> vectors while one pass covers it, else
+//             the 16-byte form below -- the batched form saves 5-20 % over
+//             the 16-byte one while it makes one pass (+ 1/16), and costs
+//             10-30 % once a fifth of its threads need a second (those
+//             threads load again only after their first loads returned, at
+//             the end of the burst).
 //  above:     16-byte groups -- W <= 2: 128 threads, U = 2, pipelined;
 //             W 3-4: 256 threads, U = 1, pipelined; W >= 5: 256 threads,
 //             U = 2 without pipelining (more loads in flight per thread).
@@ -296,7 +357,19 @@ constexpr size_t kHalfMaxElems = size_t(1) << 22;
 
 template <int W, bool kAlias>
 cudaError_t launch_policy(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
-  if (a.n <= kHalfMaxElems) return launch_half<W, 256, kAlias>(a, dev, sms, stream);
+  if (a.n <= kHalfMaxElems) {
+    bool taken = false;
+    cudaError_t err = launch_half<W, 256, 1, kAlias>(a, dev, sms, W >= 5, &taken, stream);
+    if (err != cudaSuccess || taken) return err;
+    if constexpr (kHalfU<W> > 1) {
+      err = launch_half<W, 256, kHalfU<W>, kAlias>(a, dev, sms, false, &taken, stream);
+      if (err != cudaSuccess || taken) return err;
+    }
+    if constexpr (kHalfU2<W> > 1) {
+      err = launch_half<W, 256, kHalfU2<W>, kAlias>(a, dev, sms, false, &taken, stream);
+      if (err != cudaSuccess || taken) return err;
+    }
+  }
   if constexpr (W <= 2) {
     return launch_vec<W, 128, 2, true, kAlias>(a, dev, sms, stream);
   } else if constexpr (W <= 4) {

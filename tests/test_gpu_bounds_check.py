@@ -79,10 +79,14 @@ def test_random_reduces_stay_in_bounds(checked):
     dev = torch.device("cuda:0")
     _violations(checked)
     rng = np.random.default_rng(5150)
-    sizes = [(1 << 22) - 3, (1 << 22) + 9, (1 << 23) + 5]
+    sizes = [(1 << 22) - 3, (1 << 22) + 9, (1 << 23) + 5, (1 << 21) + 5]
     for case in range(120):
         W = int(rng.integers(1, 9))
-        n = sizes[case % 3] if case % 10 == 0 else int(rng.integers(0, 5000))
+        if case % 10 == 0:
+            n = sizes[(case // 10) % 4]
+            W = 1 + (case // 10) % 4 if n == (1 << 21) + 5 else W  # the batched 8-byte form
+        else:
+            n = int(rng.integers(0, 5000))
         same = bool(rng.integers(0, 2))
         offs = [int(rng.integers(0, 8))] * (W + 1) if same else [int(v) for v in rng.integers(0, 8, W + 1)]
         alias = int(rng.integers(-1, W)) if n else -1

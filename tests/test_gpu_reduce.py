@@ -130,6 +130,29 @@ def test_both_vector_forms_ragged_misaligned_in_place(arx, dev, W, n):
     assert not buf[W - 1, 0].view(torch.int16).item() and not buf[W - 1, 1 + n:].view(torch.int16).any()
 
 
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+@pytest.mark.parametrize("n", [1_250_003, (1 << 21) + 5, 3_000_017, (1 << 22) - 1])
+@pytest.mark.parametrize("alias", [False, True])
+def test_batched_8_byte_form(arx, dev, W, n, alias):
+    # For W <= 4, sizes one pass of the one-vector grid does not cover take
+    # the batched 8-byte form (8 / W vectors per slot per thread, then twice
+    # that for W = 2, 3) while one pass of it does, else the 16-byte form.
+    # On 152 SMs: 1,250,003 elements sit just above one one-vector pass;
+    # 3,000,017 take the deeper tier at W = 3; 2^22 - 1 takes it at W = 2
+    # and the 16-byte form at W = 3, 4.  Scalar head (pointers 2 bytes past
+    # a 16-byte boundary), ragged tail, in place or not; guard elements intact.
+    x = sp.partials(W, n, "normal", seed=n % 997 + 10 * W + alias)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+    buf = torch.zeros(W + 1, n + 16, dtype=torch.bfloat16, device=dev)
+    buf[:W, 1:1 + n] = x.to(dev)
+    slots = [buf[r, 1:1 + n] for r in range(W)]
+    row = 0 if alias else W
+    arx.arx_reduce(slots, buf[row, 1:1 + n])
+    torch.cuda.synchronize()
+    assert_bits_equal(buf[row, 1:1 + n].cpu().view(torch.int16).numpy(), want, f"W={W} n={n} alias={alias}")
+    assert not buf[row, 0].view(torch.int16).item() and not buf[row, 1 + n:].view(torch.int16).any()
+
+
 def test_alias_to_last_slot(arx, dev):
     x = sp.partials(5, 40000, "normal", seed=9)
     want = oracle.reduce(list(sp.to_u16_numpy(x)))
