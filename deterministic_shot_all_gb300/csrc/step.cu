@@ -80,6 +80,15 @@ enum SyncMode : int { kSyncSemaphore = 0, kSyncPad = 1, kSyncPadFenced = 2 };
 // 16-byte vectors each thread loads before storing them while staging.
 constexpr int kStageBatch = 4;
 
+// Bytes of its input chunk a block prefetches into L2 before the dependency
+// wait: its first two staging batches.  Only for messages whose W inputs
+// total at most kPrefetchMaxBytes: there the step is latency-bound and the
+// prefetch saved 5-11 % (W = 8 [32, 4096]: 5.63 -> 5.04 us, pad barrier);
+// at 2^20 elements and above it was neutral or cost 2-4 %, competing with
+// the previous step's own traffic (A/B of two builds in one process, GB300).
+constexpr size_t kPrefetchBytes = 2u * kStageBatch * kThreads * 16u;
+constexpr size_t kPrefetchMaxBytes = size_t(4) << 20;
+
 struct Header {  // first bytes of the workspace
   uint32_t seq;        // completed steps
   uint32_t err;        // device error word
@@ -106,6 +115,7 @@ struct StepArgs {
   int fault_rank;
   uint32_t in_vec_mask;  // bit r: input r is 16-byte aligned
   int out_vec;           // out is 16-byte aligned
+  int prefetch;          // L2 prefetch of the input chunks (small messages)
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif
@@ -218,6 +228,21 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 
   __shared__ uint32_t s_seq;
   __shared__ uint32_t s_epoch;
+
+  // Chunk b (in 16-byte groups) of rank r's input.
+  const size_t G = a.n / 8u;
+  const size_t tail = a.n - 8u * G;
+  const size_t c0 = split_point(G, B, b), c1 = split_point(G, B, b + 1u);
+  const bool in_vec = (a.in_vec_mask >> r) & 1u;
+  const uint4* s4 = reinterpret_cast<const uint4*>(a.in[r]);
+  // Before waiting for the previous kernel of the stream, ask L2 for the
+  // start of this chunk, so its DRAM latency overlaps that kernel's tail.  A
+  // prefetch returns no data: inputs the previous kernel writes are still
+  // read after the wait below, through L2.
+  if (a.prefetch && tid == 0 && in_vec && c1 > c0) {
+    const size_t bytes = (c1 - c0) * 16u < kPrefetchBytes ? (c1 - c0) * 16u : kPrefetchBytes;
+    ARX_CHECKED(s4 + c0, bytes, a.in[r], a.n * 2, a.bounds_counter, prefetch_l2_bulk(s4 + c0, uint32_t(bytes)));
+  }
   dependent_launch_prologue();
 
   // 1. seq / parity; epoch check (both words loaded back to back).
@@ -231,15 +256,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     if (epoch_in != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
 
-  // Chunk b (in 16-byte groups) and the first batch of this block's staging
-  // loads.  They read only the caller's input, which no barrier guards, so
-  // they are issued before the start barrier and their DRAM latency overlaps
-  // it; the slot writes still wait for the barrier.
-  const size_t G = a.n / 8u;
-  const size_t tail = a.n - 8u * G;
-  const size_t c0 = split_point(G, B, b), c1 = split_point(G, B, b + 1u);
-  const bool in_vec = (a.in_vec_mask >> r) & 1u;
-  const uint4* s4 = reinterpret_cast<const uint4*>(a.in[r]);
+  // The first batch of this block's staging loads.  They read only the
+  // caller's input, which no barrier guards, so they are issued before the
+  // start barrier and their latency overlaps it; the slot writes still wait
+  // for the barrier.
   uint4 first[kStageBatch] = {};
   if (in_vec) {
 #pragma unroll
@@ -469,6 +489,7 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   a.fault_rank = c.fault_rank;
   for (int r = 0; r < W; ++r)
     if ((reinterpret_cast<uintptr_t>(c.in[r]) & 15u) == 0) a.in_vec_mask |= 1u << r;
+  a.prefetch = size_t(W) * c.n * 2u <= kPrefetchMaxBytes;
   a.out_vec = (reinterpret_cast<uintptr_t>(c.out) & 15u) == 0;
 
   cudaLaunchConfig_t cfg{};
