@@ -426,14 +426,18 @@ HALF_MAX_ELEMS = 1 << 22   # the library's switch from 8-byte to 16-byte vectors
 def reduce_kernel_name(W: int, n: int, alias: bool, sms: int = 152) -> str:
     """The kernel the library launches for this shape (its launch policy, restated).
 
-    Exact for the one-vector 8-byte form (W >= 5, or one pass of a grid of
-    sms x 8 blocks of 256 threads covers the n / 4 vectors, as at the
-    decode-sized workloads); larger W <= 4 messages up to 2^22 elements take
+    Exact for the one-vector 8-byte form (128 threads per block while
+    256-thread blocks would number fewer than the SMs, as at the decode-sized
+    workloads; 256 for W >= 5, or while one pass of a grid of sms x 8 blocks
+    covers the n / 4 vectors); larger W <= 4 messages up to 2^22 elements take
     a batched 8-byte form or the 16-byte one by the library's one-pass rule.
     """
     a = "true" if alias else "false"
     if n <= HALF_MAX_ELEMS:
-        if W >= 5 or -(-(n // 4) // 256) <= sms * 8:
+        blocks256 = -(-(2 * (n // 8)) // 256)
+        if blocks256 < sms:
+            return f"reduce_half_kernel<{W}, 128, 1, {a}>"
+        if W >= 5 or blocks256 <= sms * 8:
             return f"reduce_half_kernel<{W}, 256, 1, {a}>"
         return f"reduce_half_kernel<{W}, 256, U, {a}> (batched) or reduce_vec_kernel (one-pass rule)"
     if W <= 2:

@@ -342,7 +342,10 @@ cudaError_t launch_half(const VecArgs& a, int dev, int sms, bool force, bool* ta
 // Measured policy (launch-shape sweeps of W = 2, 4, 8 from 2^15 to 2^27
 // elements per partial, and a sweep of W = 1-4 from 2^20.5 to 2^22 in
 // quarter powers, on GB300, CUDA-graph replays, inputs beyond L2):
-//  n <= 2^22: the 8-byte form.  W >= 5: one vector per slot per thread.
+//  n <= 2^22: the 8-byte form, 128 threads per block while blocks of 256
+//             would number fewer than the SMs (W = 8 at 2^12 - 2^17 elements:
+//             2.6-7.3 % faster than 256; 64 threads gained less), else 256.
+//             W >= 5: one vector per slot per thread.
 //             W <= 4: one vector while one pass of the grid covers the
 //             body, else kHalfU<W> vectors while one pass covers it, else
 //             the 16-byte form below -- the batched form saves 5-20 % over
@@ -359,7 +362,13 @@ template <int W, bool kAlias>
 cudaError_t launch_policy(const VecArgs& a, int dev, int sms, cudaStream_t stream) {
   if (a.n <= kHalfMaxElems) {
     bool taken = false;
-    cudaError_t err = launch_half<W, 256, 1, kAlias>(a, dev, sms, W >= 5, &taken, stream);
+    cudaError_t err;
+    if ((2 * a.groups + 255) / 256 < size_t(sms)) {
+      // Blocks of 256 would leave SMs idle: 128-thread blocks spread the
+      // message (and its L2 prefetches) over twice as many SMs.
+      return launch_half<W, 128, 1, kAlias>(a, dev, sms, true, &taken, stream);
+    }
+    err = launch_half<W, 256, 1, kAlias>(a, dev, sms, W >= 5, &taken, stream);
     if (err != cudaSuccess || taken) return err;
     if constexpr (kHalfU<W> > 1) {
       err = launch_half<W, 256, kHalfU<W>, kAlias>(a, dev, sms, false, &taken, stream);
