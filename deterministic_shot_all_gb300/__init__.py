@@ -174,12 +174,64 @@ def _check_bf16(xs: Sequence, n: int | None, where: str, what: str) -> None:
 
 
 def _ptr_array(xs: Sequence) -> ctypes.Array:
-    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    return _ptr_array_type(len(xs))(*[_ptr(x) for x in xs])
+
+
+_ARRAY_TYPES: dict = {}
+_BF16 = None
+
+
+def _ptr_array_type(k: int):
+    t = _ARRAY_TYPES.get(k)
+    if t is None:
+        t = _ARRAY_TYPES[k] = ctypes.c_void_p * k
+    return t
+
+
+def _marshal(xs: Sequence, out, n: int, where: str, what: str, what_out: str):
+    """Checks ``xs`` and ``out`` as _check_bf16 does and returns (array of the
+    xs' addresses, out's address).  One pass over the tensors with one call
+    per property; on any failure the per-tensor checks run again to raise
+    their message."""
+    global _BF16
+    if _BF16 is None:
+        import torch
+        _BF16 = torch.bfloat16
+    cuda = where == "cuda"
+    want = None  # the current device, looked up once a tensor is on a GPU
+    addrs = []
+    for x in (*xs, out):
+        if isinstance(x, int):
+            addrs.append(x)
+            continue
+        try:
+            if x.dtype is _BF16 and x.is_contiguous() and x.numel() >= n:
+                d = x.get_device()
+                if cuda and d >= 0:
+                    if want is None:
+                        import torch
+                        want = torch.cuda.current_device()
+                    if d == want:
+                        addrs.append(x.data_ptr())
+                        continue
+                elif not cuda and d < 0:
+                    addrs.append(x.data_ptr())
+                    continue
+        except AttributeError:
+            pass
+        _check_bf16(xs, n, where, what)
+        _check_bf16([out], n, where, what_out)
+        addrs = [_ptr(y) for y in (*xs, out)]
+        break
+    return _ptr_array_type(len(xs))(*addrs[:-1]), addrs[-1]
 
 
 def _stream(stream) -> int:
     if stream is None:
         import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -202,9 +254,8 @@ def arx_reduce(slots: Sequence, out, n: int | None = None, stream=None, check: b
     raises ArxError on failure when ``check``).
     """
     n = _numel(n, out)
-    _check_bf16(slots, n, "cuda", "slots")
-    _check_bf16([out], n, "cuda", "out")
-    st = lib.arx_reduce(_ptr_array(slots), len(slots), _ptr(out), n, _stream(stream))
+    arr, optr = _marshal(slots, out, n, "cuda", "slots", "out")
+    st = lib.arx_reduce(arr, len(arr), optr, n, _stream(stream))
     if check:
         _check(st)
     return st
@@ -219,12 +270,9 @@ class arx_reduce_plan:
 
     def __init__(self, slots: Sequence, out, n: int | None = None, stream=None):
         n = _numel(n, out)
-        _check_bf16(slots, n, "cuda", "slots")
-        _check_bf16([out], n, "cuda", "out")
+        self._arr, self._out = _marshal(slots, out, n, "cuda", "slots", "out")
         self._refs = (list(slots), out)
-        self._arr = _ptr_array(slots)
         self._W = len(slots)
-        self._out = _ptr(out)
         self._n = n
         self._stream = _stream(stream)
         self._fn = lib.arx_reduce
@@ -256,10 +304,8 @@ def arx_reduce_host(host_slots: Sequence, host_out, staging=None, n: int | None 
     else:
         raise TypeError("staging must be a device tensor or None")
     n = _numel(n, host_out)
-    _check_bf16(host_slots, n, "cpu", "host_slots")
-    _check_bf16([host_out], n, "cpu", "host_out")
-    st = lib.arx_reduce_host(_ptr_array(host_slots), len(host_slots), _ptr(host_out),
-                             n, sptr, nb, _stream(stream))
+    arr, optr = _marshal(host_slots, host_out, n, "cpu", "host_slots", "host_out")
+    st = lib.arx_reduce_host(arr, len(arr), optr, n, sptr, nb, _stream(stream))
     if check:
         _check(st)
     return st
@@ -325,9 +371,8 @@ def arx_step(ctx: arx_ctx, inputs: Sequence, out, n: int | None = None, stream=N
              check: bool = True) -> int:
     """Enqueue one protocol step: out = rank-order reduce of ``inputs``."""
     n = _numel(n, out)
-    _check_bf16(inputs, n, "cuda", "inputs")
-    _check_bf16([out], n, "cuda", "out")
-    st = lib.arx_step(ctypes.byref(ctx), _ptr_array(inputs), _ptr(out), n, _stream(stream))
+    arr, optr = _marshal(inputs, out, n, "cuda", "inputs", "out")
+    st = lib.arx_step(ctypes.byref(ctx), arr, optr, n, _stream(stream))
     if check:
         _check(st)
     return st
@@ -341,12 +386,9 @@ class arx_step_plan:
 
     def __init__(self, ctx: arx_ctx, inputs: Sequence, out, n: int | None = None, stream=None):
         n = _numel(n, out)
-        _check_bf16(inputs, n, "cuda", "inputs")
-        _check_bf16([out], n, "cuda", "out")
+        self._arr, self._out = _marshal(inputs, out, n, "cuda", "inputs", "out")
         self._refs = (ctx, list(inputs), out)
         self._ctx = ctypes.byref(ctx)
-        self._arr = _ptr_array(inputs)
-        self._out = _ptr(out)
         self._n = n
         self._stream = _stream(stream)
         self._fn = lib.arx_step
@@ -393,9 +435,8 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
     receives the step's device error word.  n is limited to ARX_NOALLOC_MAX_N.
     """
     n = _numel(n, out)
-    _check_bf16(inputs, n, "cuda", "inputs")
-    _check_bf16([out], n, "cuda", "out")
-    st = lib.arx_step_noalloc(_ptr_array(inputs), len(inputs), _ptr(out), n,
+    arr, optr = _marshal(inputs, out, n, "cuda", "inputs", "out")
+    st = lib.arx_step_noalloc(arr, len(arr), optr, n,
                               _ptr(dev_status) if dev_status is not None else None, _stream(stream))
     if check:
         _check(st)
