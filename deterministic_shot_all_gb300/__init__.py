@@ -76,6 +76,8 @@ class arx_ctx(ctypes.Structure):
         ("ctrl_bytes", ctypes.c_uint64),
         ("slots", ctypes.c_void_p),
         ("slots_bytes", ctypes.c_uint64),
+        ("failed_err", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
     ]
 
 

@@ -421,17 +421,21 @@ arx_status arx_ctx_set_fault(arx_ctx* ctx, int rank) {
   return ok();
 }
 
-arx_status arx_ctx_reset(const arx_ctx* ctx, void* stream) {
+arx_status arx_ctx_reset(arx_ctx* ctx, void* stream) {
   const arx_status s = check_ctx(ctx);
   if (s != ARX_OK) return s;
   const cudaError_t e = cudaMemsetAsync(ctx->ws, 0, ctx->ctrl_bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_ctx_reset");
+  ctx->failed_err = 0;
   return ok();
 }
 
 arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, size_t n, void* stream) {
   arx_status s = check_ctx(ctx);
   if (s != ARX_OK) return s;
+  if (ctx->failed_err != 0)
+    return fail(ARX_ESTATE, "the context failed (device error word 0x%08x); arx_ctx_reset it before the next step",
+                ctx->failed_err);
   if (n == 0) return ok();
   if (n > ctx->max_n) return fail(ARX_EINVAL, "n=%zu exceeds the context's max_n=%llu", n,
                                   static_cast<unsigned long long>(ctx->max_n));
@@ -476,7 +480,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   return ok();
 }
 
-arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream) {
+arx_status arx_ctx_query(arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream) {
   const arx_status s = check_ctx(ctx);
   if (s != ARX_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -488,6 +492,7 @@ arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, v
   if (dev_err) *dev_err = words[1];
   const uint32_t code = words[1] & 0xFFu;
   if (code == 0) return ok();
+  ctx->failed_err = words[1];
   if (code == ARX_ETIMEOUT || code == ARX_ESTATE)
     return fail(static_cast<arx_status>(code), "device error word 0x%08x (stage %u, rank %u, block %u)",
                 words[1], (words[1] >> 8) & 15u, (words[1] >> 12) & 15u, words[1] >> 16);

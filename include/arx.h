@@ -176,6 +176,10 @@ typedef struct arx_ctx {
   void* slots;           /* device address of slots[2][W][slot_stride]: ws + off_slots,
                             or the separate buffer of arx_ctx_init_split */
   uint64_t slots_bytes;
+  uint32_t failed_err;   /* 0, or the nonzero device error word arx_ctx_query
+                            last read: arx_step refuses to launch (ARX_ESTATE)
+                            until arx_ctx_reset clears it */
+  uint32_t reserved;
 } arx_ctx;
 
 /* Workspace bytes for W virtual ranks, slots of max_n elements and `nblocks`
@@ -247,8 +251,9 @@ arx_status arx_ctx_set_sync(arx_ctx* ctx, int mode);
 arx_status arx_ctx_set_fault(arx_ctx* ctx, int rank);
 
 /* Enqueues a zero fill of the protocol words [0, ctrl_bytes) (not the slots):
- * seq, epochs, Semaphores, pad and the error word all return to zero. */
-arx_status arx_ctx_reset(const arx_ctx* ctx, void* stream);
+ * seq, epochs, Semaphores, pad and the error word all return to zero; clears
+ * ctx->failed_err, so steps may be launched again. */
+arx_status arx_ctx_reset(arx_ctx* ctx, void* stream);
 
 /* One protocol step: out = rank-order reduce of inputs[0..W-1].
  *   inputs  HOST array of ctx->W device pointers, each to n bf16 elements;
@@ -256,14 +261,18 @@ arx_status arx_ctx_reset(const arx_ctx* ctx, void* stream);
  *   out     device pointer to n bf16; may equal one input exactly; must not
  *           overlap the protocol words or the slots.
  *   n       0 < n <= ctx->max_n (n == 0 returns ARX_OK, no launch).
- * Steps on one context must be serialised (one stream, or events). */
+ * Steps on one context must be serialised (one stream, or events).  Like the
+ * pages' error flag checked before every launch: once arx_ctx_query has read
+ * a device error (ctx->failed_err != 0), arx_step returns ARX_ESTATE without
+ * launching until arx_ctx_reset. */
 arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, size_t n,
                     void* stream);
 
 /* Synchronises `stream`, then reads the header: *seq = completed steps,
  * *dev_err = device error word (either pointer may be NULL).  Returns the
- * status in the error word's low 8 bits (ARX_OK when it is 0), or ARX_ECUDA. */
-arx_status arx_ctx_query(const arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream);
+ * status in the error word's low 8 bits (ARX_OK when it is 0), or ARX_ECUDA.
+ * A nonzero error word is also kept in ctx->failed_err (see arx_step). */
+arx_status arx_ctx_query(arx_ctx* ctx, uint32_t* seq, uint32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Bounds checks.  The library can be built a second way, with every data

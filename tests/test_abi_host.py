@@ -154,6 +154,26 @@ def test_ctx_knobs_and_step_validation(arx):
     assert arx.lib.arx_step(ctypes.byref(ctx), bad, FAKE + (1 << 34), n, None) == arx.ARX_EINVAL
 
 
+def test_failed_context_refuses_to_launch(arx):
+    # The pages check an error flag before every launch; here the flag is the
+    # device error word arx_ctx_query last read, kept in the host struct.
+    # arx_step must refuse before any CUDA call (none can run on this host).
+    W, n, B = 4, 4096, 2
+    ctx = arx.arx_ctx()
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, arx.arx_ctx_workspace_bytes(W, n, B), W, n, B) == 0
+    assert ctx.failed_err == 0
+    ins = (ctypes.c_void_p * W)(*[FAKE + (1 << 32) + i * (1 << 20) for i in range(W)])
+    ctx.failed_err = 0x00120204  # ETIMEOUT at the end wait, rank 2, block 18
+    assert arx.lib.arx_step(ctypes.byref(ctx), ins, FAKE + (1 << 34), n, None) == arx.ARX_ESTATE
+    assert "0x00120204" in arx.arx_last_error() and "arx_ctx_reset" in arx.arx_last_error()
+    with pytest.raises(arx.ArxError):
+        arx.arx_step(ctx, [FAKE + (1 << 32) + i * (1 << 20) for i in range(W)], FAKE + (1 << 34), n, stream=0)
+    # Even an empty step is refused, and re-initialising clears the flag.
+    assert arx.lib.arx_step(ctypes.byref(ctx), ins, FAKE + (1 << 34), 0, None) == arx.ARX_ESTATE
+    assert arx.lib.arx_ctx_init(ctypes.byref(ctx), FAKE, arx.arx_ctx_workspace_bytes(W, n, B), W, n, B) == 0
+    assert ctx.failed_err == 0
+
+
 def test_split_layout_and_rejections(arx):
     W, n, B = 8, 131072, 19
     words = arx.arx_ctx_words_bytes(W, B)

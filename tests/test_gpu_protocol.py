@@ -345,9 +345,20 @@ def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
     assert w["blocks"] == [0, 0]
     if sync == "semaphore":
         assert not w["pad"].any()
-    # Recovery: zero the protocol words, clear the fault, step again.
+    # The context remembers the failure: the next step is refused on the host,
+    # with nothing launched (output and protocol words untouched).
+    assert c.ctx.failed_err == err
     arx.arx_ctx_set_fault(c.ctx, -1)
+    sentinel = torch.full((n,), 7.0, dtype=torch.bfloat16, device=dev)
+    xd = x.to(dev)
+    words_before = c.ws[:c.ctx.ctrl_bytes].clone()
+    assert arx.arx_step(c.ctx, [xd[r] for r in range(W)], sentinel, check=False) == arx.ARX_ESTATE
+    torch.cuda.synchronize()
+    assert bool((sentinel == 7.0).all())
+    assert torch.equal(c.ws[:c.ctx.ctrl_bytes], words_before)
+    # Recovery: zero the protocol words, step again.
     arx.arx_ctx_reset(c.ctx)
+    assert c.ctx.failed_err == 0
     out = _step(arx, c, x, dev)
     assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, 1, 0)
     assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
