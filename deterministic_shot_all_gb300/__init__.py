@@ -402,7 +402,11 @@ class arx_step_plan:
 
 
 def arx_ctx_query(ctx: arx_ctx, stream=None) -> tuple[int, int, int]:
-    """Synchronise ``stream``; return (status, completed seq, device error word)."""
+    """Synchronise ``stream``; return (status, completed seq, device error word).
+
+    A nonzero error word is also kept in ``ctx.failed_err``: later
+    ``arx_step`` calls on the context return ARX_ESTATE without launching
+    until ``arx_ctx_reset``."""
     seq = ctypes.c_uint32(0)
     err = ctypes.c_uint32(0)
     st = lib.arx_ctx_query(ctypes.byref(ctx), ctypes.byref(seq), ctypes.byref(err), _stream(stream))
