@@ -673,7 +673,8 @@ def stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R) -> dict:
 
     back_to_back: K calls enqueued in a row, events around the batch (bound by the
     host's launch rate); single_call: events around one call at a time, GPU idle
-    before each, median over the calls (includes the launch latency).
+    before each, median over the calls (includes the launch latency); the plan_
+    figures: the same through a prepared arx_reduce_plan (one C call per call).
     """
     def call(i):
         arx.arx_reduce(slot_lists[i % R], outs[i % R], stream=stream)
@@ -713,9 +714,19 @@ def stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R) -> dict:
         e.record(stream)
         torch.cuda.synchronize()
         b2b_plan = s.elapsed_time(e) / 1e3 / K
+        single_plan = []
+        for i in range(1000):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            plans[i % R]()
+            e.record(stream)
+            e.synchronize()
+            single_plan.append(s.elapsed_time(e) / 1e3)
     return {"back_to_back_us_per_call": b2b * 1e6, "calls": K,
             "single_call_us_median": statistics.median(single) * 1e6, "single_calls": len(single),
-            "plan_back_to_back_us_per_call": b2b_plan * 1e6}
+            "plan_back_to_back_us_per_call": b2b_plan * 1e6,
+            "plan_single_call_us_median": statistics.median(single_plan) * 1e6}
 
 
 def hot_l2_point(torch, arx, stream, slot_lists, outs, W, n) -> dict:
