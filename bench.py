@@ -41,6 +41,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -108,12 +109,19 @@ def measured_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the reduce kernel's sources: ties a stored ncu traffic figure to this code."""
+    """Hash of the reduce kernel's sources: ties a stored ncu traffic figure to this code.
+
+    Comments and whitespace are left out, so editing a comment keeps the
+    figure; any change to the code itself gives a new hash.
+    """
     h = hashlib.sha256()
     for rel in ("deterministic_shot_all_gb300/csrc/reduce.cu",
                 "deterministic_shot_all_gb300/csrc/arx_device.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                  # line comments
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

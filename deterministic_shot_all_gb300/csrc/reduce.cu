@@ -14,6 +14,9 @@
 //    8-byte vectors (4 elements) per slot, one per thread per iteration --
 //    twice the threads of the 16-byte form at half the registers each, so
 //    more loads are in flight per SM and the message spreads over more SMs;
+//    128-thread blocks while 256-thread ones would leave SMs idle; for
+//    W <= 4, 8/W (then 16/W) vectors per thread while that keeps the
+//    message within one pass of the grid (see launch_policy);
 //  * above (bandwidth-bound): 16-byte vectors, U independent groups per
 //    thread per iteration, all W*U loads issued before the first add
 //    (Little's law against HBM3e latency);
