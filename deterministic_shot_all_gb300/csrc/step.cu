@@ -246,13 +246,12 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   dependent_launch_prologue();
 
   // 1. seq / parity; epoch check (both words loaded back to back).
-  uint32_t epoch_in = 0;  // thread 0 only
   if (tid == 0) {
     const uint32_t done = ld_relaxed_gpu(&hdr->seq);
-    epoch_in = epoch[r * B + b];
+    const uint32_t epoch_in = epoch[r * B + b];
     const uint32_t seq = done + 1u;
     s_seq = seq;
-    if constexpr (kPad) s_epoch = epoch_in;
+    s_epoch = epoch_in;
     if (epoch_in != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
 
@@ -414,32 +413,19 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // 6. exit: zero-resetting pad barrier (Pattern 2: block barrier, then the
   // barrier -- relaxed, or acq_rel in the fenced variant), then the epoch
   // flip and the block-out count.  No block of this launch reads those two
-  // words (later kernels and the host see them after the kernel ends), so in
-  // the pad variants a thread outside the barrier does them concurrently with
-  // it (5.6 instead of 6.3 us per step); in the Semaphore variant the same
-  // change measured slower, so there they follow the barrier.
+  // words (later kernels and the host see them after the kernel ends), so a
+  // thread outside the barrier does them concurrently with it: pad variant
+  // 6.3 -> 5.6 us per step, Semaphore variant 6.46 -> 6.01 us (W = 8
+  // [32, 4096], A/B of two builds in one process, the same on two GPUs).
   __syncthreads();
-  if constexpr (kPad) {
-    if (tid < uint32_t(W)) {
-      pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
-                              kPadWait);
-    } else if (tid == 32u) {
-      epoch[r * B + b] = (s_epoch + 1u) % 2u;  // PushController::exit
-      if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
-        hdr->blocks[1] = 0u;
-        st_relaxed_gpu(&hdr->seq, seq);
-      }
-    }
-  } else {
-    if (tid < uint32_t(W))
-      pad_barrier<false>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend, kPadWait);
-    __syncthreads();
-    if (tid == 0) {
-      epoch[r * B + b] = (epoch_in + 1u) % 2u;  // PushController::exit
-      if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
-        hdr->blocks[1] = 0u;
-        st_relaxed_gpu(&hdr->seq, seq);
-      }
+  if (tid < uint32_t(W)) {
+    pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
+                            kPadWait);
+  } else if (tid == 32u) {
+    epoch[r * B + b] = (s_epoch + 1u) % 2u;  // PushController::exit
+    if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
+      hdr->blocks[1] = 0u;
+      st_relaxed_gpu(&hdr->seq, seq);
     }
   }
 }
