@@ -294,6 +294,20 @@ int auto_blocks(int W, size_t max_n, arx_status* s) {
   return int(B);
 }
 
+// Block groups of the staggered staging for slots in host memory: about
+// 128 KiB of staged data per group (the link writes that in about the time
+// one group's hand-off to the next takes), at most 16 and at most B; 0 (all
+// at once) below two.  Measured on GB300 over NVLink-C2C (W = 8
+// [32, 4096]: 25.6 us per step at once, 20.3-20.9 at 16 groups; W = 4:
+// 14.5 -> 11.8-12.2 us at 8 groups; W = 8 at 2^19: 85 -> 61 us at 16).
+int stagger_groups(int W, size_t n, int B) {
+  const size_t bytes = size_t(W) * n * 2;
+  size_t K = (bytes + (size_t(64) << 10)) >> 17;  // nearest multiple of 128 KiB
+  if (K > 16) K = 16;
+  if (K > size_t(B)) K = size_t(B);
+  return K < 2 ? 0 : int(K);
+}
+
 arx_status check_ctx(const arx_ctx* ctx) {
   if (!ctx || ctx->magic != kCtxMagic) return fail(ARX_ESTATE, "context not initialised");
   return ARX_OK;
@@ -474,6 +488,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.B = ctx->nblocks;
   c.fault_rank = ctx->fault_rank;
   c.sync_mode = ctx->sync_mode;
+  c.stagger = ctx->slots_where == ARX_SLOTS_HOST ? stagger_groups(ctx->W, n, ctx->nblocks) : 0;
   ARX_SET_BOUNDS_COUNTER(c);
   e = arx::launch_step(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_step launch");

@@ -45,6 +45,7 @@ struct StepCall {
   int W, B;
   int fault_rank;
   int sync_mode;  // ARX_SYNC_*
+  int stagger;    // K >= 2: K block groups start staging in turn (slots in host memory); else 0
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif

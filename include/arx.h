@@ -147,7 +147,9 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  * nblocks) bytes and 256-byte aligned.  Layout (offsets in arx_ctx):
  *   [0, 256)        header, uint32: seq (completed steps), err (device error
  *                   word, 0 = none), blocks[2] (publish / exit counters),
- *                   published (last staged seq)
+ *                   published (last staged seq); at byte 128
+ *                   stagger[2][16] (staging-done counts of a staggered
+ *                   host-slot step, zero between steps)
  *   off_epoch       uint32 epoch[W][B]                    (PushController)
  *   off_sem         struct { uint32 flag, counter; } sem[W][B], 128-byte
  *                   stride                                (Semaphore)
@@ -156,8 +158,8 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  * Device error word: low 8 bits an arx_status, bits 8-11 the stage that
  * failed (1 start Semaphore wait, 2 end Semaphore wait, 3 exit pad send,
  * 4 exit pad wait, 5 epoch check, 6 start pad send, 7 start pad wait, 8 end
- * pad send, 9 end pad wait), bits 12-15 the virtual rank, bits 16-31 the
- * block.
+ * pad send, 9 end pad wait, 10 staggered-staging wait), bits 12-15 the
+ * virtual rank, bits 16-31 the block.
  * ------------------------------------------------------------------------- */
 typedef struct arx_ctx {
   uint32_t magic;        /* set by arx_ctx_init */
@@ -210,7 +212,13 @@ arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t m
  *                  torch pin_memory); the library looks up its device
  *                  address (ARX_EINVAL if it is not page-locked).
  * Everything else as arx_ctx_init; arx_ctx_reset zeroes the words only.
- * Buffers are the caller's and must outlive the context's last step. */
+ * Buffers are the caller's and must outlive the context's last step.
+ * With the slots in host memory a step of at least 192 KiB of partials
+ * stages in turn: its blocks form up to 16 groups by chunk (about 128 KiB of
+ * staged data each), and each group starts writing its slots once every
+ * block of the previous group has issued its own, so writes to host memory
+ * overlap the previous group's reads on the full-duplex link.  Only the
+ * start times move; barriers and result are the same. */
 #define ARX_SLOTS_DEVICE 0
 #define ARX_SLOTS_HOST 1
 size_t arx_ctx_words_bytes(int W, int nblocks);

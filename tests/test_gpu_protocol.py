@@ -80,7 +80,8 @@ class Ctx:
         hdr = u32(0, 5)
         sem = host[c.off_sem: c.off_sem + 128 * W * B].reshape(W * B, 128)[:, :8].copy().view(np.uint32)
         return dict(seq=int(hdr[0]), err=int(hdr[1]), blocks=[int(hdr[2]), int(hdr[3])],
-                    published=int(hdr[4]), epoch=u32(c.off_epoch, W * B).reshape(W, B),
+                    published=int(hdr[4]), stagger=u32(128, 32).reshape(2, 16),
+                    epoch=u32(c.off_epoch, W * B).reshape(W, B),
                     flag=sem[:, 0].astype(np.int64).reshape(W, B),
                     counter=sem[:, 1].astype(np.int64).reshape(W, B),
                     pad=u32(c.off_pad, W * B * W).reshape(W, B, W))
@@ -96,6 +97,13 @@ class Ctx:
 
     def poke(self, off, value):
         self.ws[off: off + 4] = torch.tensor([value], dtype=torch.int64).view(torch.uint8)[:4].to(self.ws.device)
+
+
+def _stagger_groups(W, n, B):
+    """Block groups of a host-slot step: about 128 KiB of staged data each,
+    at most 16 and at most B; none below two (as include/arx.h describes)."""
+    K = min((W * n * 2 + (64 << 10)) >> 17, 16, B)
+    return K if K >= 2 else 0
 
 
 def _compare_to_model(words, st: model.State):
@@ -149,6 +157,28 @@ def test_single_step_host_slots(arx, dev, W):
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
                           f"host slots W={W} n={n} B={c.B}")
         assert np.array_equal(c.slot(1, W - 1, n), sp.to_u16_numpy(x)[W - 1])
+
+
+def test_host_slot_steps_of_varying_size(arx, dev):
+    # Slots in host memory: steps of 192 KiB of partials or more stage in
+    # turn, in a number of block groups that follows each step's size; smaller
+    # ones all at once.  Mixing them on one context must not matter: every
+    # output bit-exact, the staging counts back to zero after every step.
+    W, max_n = 8, 131072
+    c = Ctx(arx, dev, W, max_n, 0, "semaphore", "host")
+    staggered = 0
+    for s, n in enumerate((131072, 4096, 70001, 131072, 11, 65536)):
+        for sync in SYNCS:
+            arx.arx_ctx_set_sync(c.ctx, SYNCS.index(sync))
+            x = sp.partials(W, n, "normal", seed=700 + 10 * s + SYNCS.index(sync))
+            out = _step(arx, c, x, dev)
+            st, seq, err = arx.arx_ctx_query(c.ctx)
+            assert (st, err) == (arx.ARX_OK, 0)
+            assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
+                              f"n={n} {sync}")
+            staggered += bool(_stagger_groups(W, n, c.B))
+            assert not c.words()["stagger"].any(), (n, sync, seq)
+    assert staggered > 0
 
 
 def test_random_small_steps(arx, dev):
@@ -294,6 +324,9 @@ def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync, slots):
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s}")
         _compare_to_model(c.words(), st)
     assert (c.words()["flag"] == (2 * W * k if sync == "semaphore" else 0)).all()
+    # Staggered staging counts: zero between steps (the last block out of a
+    # staggered step clears its bank), host slots or not.
+    assert not c.words()["stagger"].any()
     for r in range(W):
         assert np.array_equal(c.slot(k & 1, r, n), hist[k - 1][r])
         if k >= 2:
@@ -530,6 +563,7 @@ def test_ten_thousand_steps_in_one_graph(arx, dev, graph_workload, sync, slots):
     assert (w["flag"] == flags).all() and (w["counter"] == w["flag"]).all()
     assert (w["epoch"] == steps % 2).all() and w["blocks"] == [0, 0]
     assert w["published"] == steps
+    assert not w["stagger"].any()
     for r in range(W8):
         assert np.array_equal(c.slot(steps & 1, r, N8), last_two[steps - 1][r])
         assert np.array_equal(c.slot((steps - 1) & 1, r, N8), last_two[steps - 2][r])
