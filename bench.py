@@ -623,8 +623,9 @@ def protocol_graph_point(torch, arx, sp, dev, stream) -> dict:
 def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link) -> dict:
     """arx_step with the slot banks in page-locked host memory (arx_ctx_init_split):
     every step writes the W staged partials to host memory and reads them back
-    over NVLink-C2C.  Link roofline: the time the measured pinned copy rates
-    need to move those bytes out and back."""
+    over NVLink-C2C.  Link roofline: the time the measured rate of pinned
+    copies in both directions at once needs to move those bytes out and back
+    (and, for reference, the one-way rates one after the other)."""
     W, n = 8, sp.N_32x4096
     x, _ = sp.workload(workload)
     R = rotation_sets(W * n * 2 * 2, l2)
@@ -643,13 +644,16 @@ def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link) -
     t = timed_graph_calls(torch, stream, call, steps, 10) / steps
     st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
     moved = W * n * 2
-    t_link = moved / (link["d2h"] * 1e9) + moved / (link["h2d"] * 1e9)
+    t_serial = moved / (link["d2h"] * 1e9) + moved / (link["h2d"] * 1e9)
+    t_duplex = 2 * moved / (link["both"] * 1e9)
     return {"W": W, "n": n, "steps": steps, "blocks_per_rank": ctx.nblocks, "us_per_step": t * 1e6,
             "status": arx.arx_status_string(st), "seq": seq,
             "link_bytes_per_step": 2 * moved,
-            "roofline": {"bound": "c2c", "link_bound_us": t_link * 1e6, "frac": t_link / t,
-                         "basis": "staged bytes out at the measured pinned D2H rate plus back at the "
-                                  "measured H2D rate, serially"}}
+            "roofline": {"bound": "c2c", "link_bound_us": t_duplex * 1e6, "frac": t_duplex / t,
+                         "basis": "staged bytes out and back at the measured rate of pinned copies in "
+                                  "both directions at once (the steps stage in turn, so writes and "
+                                  "reads overlap)",
+                         "serial_bound_us": t_serial * 1e6, "serial_frac": t_serial / t}}
 
 
 def pinned_copy_gbs(torch, dev, nbytes: int = 1 << 26, reps: int = 5) -> dict:
@@ -672,6 +676,27 @@ def pinned_copy_gbs(torch, dev, nbytes: int = 1 << 26, reps: int = 5) -> dict:
             torch.cuda.synchronize()
             best = min(best, s.elapsed_time(e) / 1e3)
         out[name] = nbytes / best / 1e9
+    # Both directions at once (two streams, one copy each way): the link's
+    # full-duplex rate, total bytes over the time both take.
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    best = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(s1)
+        s2.wait_event(s)
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+        s1.wait_stream(s2)
+        e.record(s1)
+        torch.cuda.synchronize()
+        best = min(best, s.elapsed_time(e) / 1e3)
+    out["both"] = 2 * nbytes / best / 1e9
     out["bytes"] = nbytes
     return out
 
