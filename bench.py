@@ -432,15 +432,17 @@ HALF_MAX_ELEMS = 1 << 22   # the library's switch from 8-byte to 16-byte vectors
 
 
 def reduce_kernel_name(W: int, n: int, alias: bool, sms: int = 152) -> str:
-    """The kernel the library launches for this shape (its launch policy, restated).
+    """The kernel the library launches for this shape (its launch policy,
+    restated), with its template arguments as ncu prints them (bools as 0/1).
 
     Exact for the one-vector 8-byte form (128 threads per block while
     256-thread blocks would number fewer than the SMs, as at the decode-sized
     workloads; 256 for W >= 5, or while one pass of a grid of sms x 8 blocks
-    covers the n / 4 vectors); larger W <= 4 messages up to 2^22 elements take
-    a batched 8-byte form or the 16-byte one by the library's one-pass rule.
+    covers the n / 4 vectors) and for the 16-byte form above 2^22 elements;
+    W <= 4 messages between take a batched 8-byte form or the 16-byte one by
+    the library's one-pass rule.
     """
-    a = "true" if alias else "false"
+    a = int(alias)
     if n <= HALF_MAX_ELEMS:
         blocks256 = -(-(2 * (n // 8)) // 256)
         if blocks256 < sms:
@@ -449,10 +451,10 @@ def reduce_kernel_name(W: int, n: int, alias: bool, sms: int = 152) -> str:
             return f"reduce_half_kernel<{W}, 256, 1, {a}>"
         return f"reduce_half_kernel<{W}, 256, U, {a}> (batched) or reduce_vec_kernel (one-pass rule)"
     if W <= 2:
-        return f"reduce_vec_kernel<{W}, 128, 2, pipelined, {a}>"
+        return f"reduce_vec_kernel<{W}, 128, 2, 1, {a}>"
     if W <= 4:
-        return f"reduce_vec_kernel<{W}, 256, 1, pipelined, {a}>"
-    return f"reduce_vec_kernel<{W}, 256, 2, {a}>"
+        return f"reduce_vec_kernel<{W}, 256, 1, 1, {a}>"
+    return f"reduce_vec_kernel<{W}, 256, 2, 0, {a}>"
 
 
 def bandwidth_points(torch, arx, sp, dev, stream, l2) -> list:
