@@ -133,7 +133,9 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  * B x W thread blocks, block (b, r) playing rank r's block b:
  *   1. seq = completed + 1, par = seq & 1; check epoch[r][b] == (seq-1) & 1;
  *   2. start barrier (unfenced): +1 to sem[q][b] for every q, wait for W;
- *   3. stage input r's chunk b into slots[par][r]; last block publishes seq;
+ *   3. stage input r's chunk b into slots[par][r]; last block publishes seq
+ *      (slots in host memory: block groups start staging in turn, see
+ *      arx_ctx_init_split);
  *   4. end barrier (release/acquire): +1 to sem[q][b], wait for 2W, counter += 2W;
  *   5. reduce sub-range r of chunk b over slots[par][0..W-1] into out;
  *   6. pad barrier (0->1 sends, 1->0 waits), epoch[r][b] ^= 1, last block out
