@@ -513,12 +513,13 @@ def floor_point(torch, arx, dev, stream, l2, W, n, per_call) -> dict:
             "marginal_GBs": gbs((W + 1) * n * 2, above) if above > 0 else None}
 
 
-SYNC_MODES = ("semaphore", "pad", "pad_fenced")
+SYNC_MODES = ("semaphore", "pad", "pad_fenced", "cluster")
 
 
 def protocol_point(torch, arx, sp, dev, stream, l2, workload, steps: int = 2000) -> dict:
     """arx_step per step (W=8, [32,4096]) in captured graphs, fresh input sets rotating,
-    for each barrier variant (Semaphore barriers; pad barrier Patterns 0/1/2; all acq_rel)."""
+    for each barrier variant (Semaphore barriers; pad barrier Patterns 0/1/2; all acq_rel;
+    the thread-block cluster barrier)."""
     W, n = 8, sp.N_32x4096
     x, _ = sp.workload(workload)
     R = rotation_sets(W * n * 2 * 2, l2)

@@ -33,7 +33,7 @@ ARX_MAX_W = 8
 ARX_STEP_MAX_BLOCKS = 256
 ARX_DEFAULT_TIMEOUT_NS = 1_000_000_000
 ARX_NOALLOC_MAX_N = 131072
-ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED = range(3)
+ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED, ARX_SYNC_CLUSTER = range(4)
 ARX_SLOTS_DEVICE, ARX_SLOTS_HOST = range(2)
 
 
@@ -357,7 +357,8 @@ def arx_ctx_set_timeout(ctx: arx_ctx, ns: int) -> None:
 
 
 def arx_ctx_set_sync(ctx: arx_ctx, mode: int) -> None:
-    """Barrier variant of later steps: ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD or ARX_SYNC_PAD_FENCED."""
+    """Barrier variant of later steps: ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD,
+    ARX_SYNC_PAD_FENCED or ARX_SYNC_CLUSTER."""
     _check(lib.arx_ctx_set_sync(ctypes.byref(ctx), int(mode)))
 
 

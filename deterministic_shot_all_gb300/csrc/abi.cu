@@ -421,7 +421,8 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns) {
 arx_status arx_ctx_set_sync(arx_ctx* ctx, int mode) {
   const arx_status s = check_ctx(ctx);
   if (s != ARX_OK) return s;
-  if (mode != ARX_SYNC_SEMAPHORE && mode != ARX_SYNC_PAD && mode != ARX_SYNC_PAD_FENCED)
+  if (mode != ARX_SYNC_SEMAPHORE && mode != ARX_SYNC_PAD && mode != ARX_SYNC_PAD_FENCED &&
+      mode != ARX_SYNC_CLUSTER)
     return fail(ARX_EINVAL, "unknown sync mode %d", mode);
   ctx->sync_mode = mode;
   return ok();
@@ -453,8 +454,10 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   if (n == 0) return ok();
   if (n > ctx->max_n) return fail(ARX_EINVAL, "n=%zu exceeds the context's max_n=%llu", n,
                                   static_cast<unsigned long long>(ctx->max_n));
-  if (ctx->sync_mode < ARX_SYNC_SEMAPHORE || ctx->sync_mode > ARX_SYNC_PAD_FENCED)
+  if (ctx->sync_mode < ARX_SYNC_SEMAPHORE || ctx->sync_mode > ARX_SYNC_CLUSTER)
     return fail(ARX_ESTATE, "context holds an unknown sync mode %d", ctx->sync_mode);
+  if (ctx->sync_mode == ARX_SYNC_CLUSTER && ctx->fault_rank >= 0)
+    return fail(ARX_EINVAL, "fault injection skips a flag signal; the cluster barrier has none to skip");
   bool alias = false;
   s = check_io(inputs, ctx->W, out, n, &alias);
   if (s != ARX_OK) return s;
@@ -488,7 +491,9 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.B = ctx->nblocks;
   c.fault_rank = ctx->fault_rank;
   c.sync_mode = ctx->sync_mode;
-  c.stagger = ctx->slots_where == ARX_SLOTS_HOST ? stagger_groups(ctx->W, n, ctx->nblocks) : 0;
+  c.stagger = ctx->slots_where == ARX_SLOTS_HOST && ctx->sync_mode != ARX_SYNC_CLUSTER
+                  ? stagger_groups(ctx->W, n, ctx->nblocks)
+                  : 0;
   ARX_SET_BOUNDS_COUNTER(c);
   e = arx::launch_step(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_step launch");

@@ -185,6 +185,26 @@ __device__ __forceinline__ void dependent_launch_prologue() {
   asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
+// ---- thread-block cluster barrier ------------------------------------------------
+//
+// Every thread of every block of the cluster arrives, then waits for all of
+// them (hardware barrier; `.aligned`: all threads of a warp execute it
+// together).  Arrive with release orders the arriving thread's earlier
+// writes -- and, after a block barrier, its block's -- before the waits of
+// the other blocks, which acquire them.
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- scoped atomics and loads for the protocol words (one GPU: .gpu scope) -------
 
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {

@@ -76,7 +76,7 @@ enum Stage : uint32_t {
 };
 
 // Barrier variants (arx.h, ARX_SYNC_*).
-enum SyncMode : int { kSyncSemaphore = 0, kSyncPad = 1, kSyncPadFenced = 2 };
+enum SyncMode : int { kSyncSemaphore = 0, kSyncPad = 1, kSyncPadFenced = 2, kSyncCluster = 3 };
 
 // 16-byte vectors each thread loads before storing them while staging.
 constexpr int kStageBatch = 4;
@@ -230,7 +230,8 @@ __device__ __forceinline__ size_t split_point(size_t total, uint32_t parts, uint
 
 template <int W, int kSync, bool kStagger>
 __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
-  constexpr bool kPad = kSync != kSyncSemaphore;
+  constexpr bool kPad = kSync == kSyncPad || kSync == kSyncPadFenced;
+  constexpr bool kCluster = kSync == kSyncCluster;  // grid clusters of (1, W, 1)
   constexpr bool kFencedAll = kSync == kSyncPadFenced;
   const uint32_t b = blockIdx.x, r = blockIdx.y;
   const uint32_t B = uint32_t(a.B);
@@ -287,7 +288,11 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // 2. start barrier.
   Semaphore& own = sem[r * B + b];
   uint32_t base = 0;
-  if constexpr (!kPad) {
+  if constexpr (kCluster) {
+    // The W blocks of chunk b are one cluster: its hardware barrier, relaxed.
+    cluster_arrive_relaxed();
+    cluster_wait();
+  } else if constexpr (!kPad) {
     // PullController start stage, unfenced: no block barrier before the signal.
     if (lane == 0 && warp < uint32_t(W)) {
       red_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
@@ -374,7 +379,17 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   if constexpr (kStagger) {
     if (grp + 1u < K && tid == uint32_t(kThreads) - 1u) red_add_relaxed_gpu(&hdr->stagger[par][grp], 1u);
   }
-  if constexpr (kPad) {
+  if constexpr (kCluster) {
+    // Release on arrive (after the block barrier: the whole block's staging),
+    // acquire on wait; the published count runs between the two.
+    cluster_arrive_release();
+    if (tid == 32u && atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
+      hdr->blocks[0] = 0u;
+      st_relaxed_gpu(&hdr->published, seq);
+    }
+    __syncwarp();
+    cluster_wait();
+  } else if constexpr (kPad) {
     // Pattern 1: block sync, acq_rel barrier, block sync.
     if (tid < uint32_t(W)) {
       pad_barrier<true>(pad, B, uint32_t(W), b, r, tid, int(r) != a.fault_rank, a.timeout_ns, &hdr->err,
@@ -463,7 +478,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // 6.3 -> 5.6 us per step, Semaphore variant 6.46 -> 6.01 us (W = 8
   // [32, 4096], A/B of two builds in one process, the same on two GPUs).
   __syncthreads();
-  if (tid < uint32_t(W)) {
+  if constexpr (kCluster) cluster_arrive_relaxed();
+  if (!kCluster && tid < uint32_t(W)) {
     pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
                             kPadWait);
   } else if (tid == 32u) {
@@ -482,6 +498,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       st_relaxed_gpu(&hdr->seq, seq);
     }
   }
+  if constexpr (kCluster) {
+    __syncwarp();
+    cluster_wait();
+  }
 }
 
 constexpr int kMaxDevices = 64;
@@ -497,9 +517,10 @@ int blocks_per_sm(int dev, cudaError_t* err) {
     if (c > 0) return c;
   }
   int lo = 0;
-  const void* kernels[6] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+  const void* kernels[7] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, true>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, true>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, true>)};
@@ -569,6 +590,21 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
       err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPadFenced, true>, a)
                : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPadFenced, false>, a);
       break;
+    case kSyncCluster: {
+      // The W blocks of a chunk form one cluster and wait only on each
+      // other (no staggered staging in this variant): clusters need not be
+      // resident together, so no cooperative launch.
+      cudaLaunchAttribute cattr[2];
+      cattr[0].id = cudaLaunchAttributeClusterDimension;
+      cattr[0].val.clusterDim.x = 1;
+      cattr[0].val.clusterDim.y = unsigned(W);
+      cattr[0].val.clusterDim.z = 1;
+      cattr[1] = attr[1];
+      cfg.attrs = cattr;
+      cfg.numAttrs = 2;
+      err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncCluster, false>, a);
+      break;
+    }
     default: break;
   }
   if (err != cudaSuccess) return err;

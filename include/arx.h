@@ -244,11 +244,21 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
  *                       (relaxed) at exit.  The Semaphores stay untouched.
  *  ARX_SYNC_PAD_FENCED  as ARX_SYNC_PAD with acq_rel compare-and-swaps in all
  *                       three barriers.
+ *  ARX_SYNC_CLUSTER     no counterpart on the pages, which synchronise
+ *                       separate GPUs: the W blocks of a chunk are one
+ *                       thread-block cluster and each of the three barriers
+ *                       is the cluster's hardware barrier (relaxed at start
+ *                       and exit; release on arrive, acquire on wait after
+ *                       staging).  Semaphores and pad are left alone; seq,
+ *                       epochs and the counters advance as in the others.
+ *                       The fault-injection knob is refused (ARX_EINVAL) and
+ *                       slots in host memory are staged all at once.
  * After every completed step the pad is all zero in every mode; in the pad
- * modes the Semaphore flags and counters keep their values. */
+ * and cluster modes the Semaphore flags and counters keep their values. */
 #define ARX_SYNC_SEMAPHORE 0
 #define ARX_SYNC_PAD 1
 #define ARX_SYNC_PAD_FENCED 2
+#define ARX_SYNC_CLUSTER 3
 
 /* Selects the barrier variant of later steps (ARX_EINVAL for an unknown
  * mode).  Switching between steps is allowed: every mode leaves the pad all

@@ -103,7 +103,7 @@ def _set_err(st: State, code: int) -> None:
         st.err = code
 
 
-SYNC_MODES = ("semaphore", "pad", "pad_fenced")
+SYNC_MODES = ("semaphore", "pad", "pad_fenced", "cluster")
 
 
 def _pad_barrier(st: State, skip_rank: int | None = None) -> None:
@@ -142,7 +142,13 @@ def step(st: State, inputs, skip_end_signal_rank: int | None = None,
         raise ValueError("need one input per virtual rank")
     if sync not in SYNC_MODES:
         raise ValueError(f"unknown sync mode {sync!r}")
-    pad_mode = sync != "semaphore"
+    # "cluster": the single-GPU reading in which the W blocks of a chunk form
+    # one thread-block cluster and every barrier is its hardware barrier --
+    # no protocol word takes part, and there is no signal to skip.
+    cluster = sync == "cluster"
+    if cluster and skip_end_signal_rank is not None:
+        raise ValueError("the cluster barrier has no signal to skip")
+    pad_mode = sync in ("pad", "pad_fenced")
     inputs = [np.ascontiguousarray(np.asarray(x, dtype=np.uint16)).reshape(-1) for x in inputs]
 
     # 1. seq / parity, and the per-block epoch check.
@@ -154,7 +160,9 @@ def step(st: State, inputs, skip_end_signal_rank: int | None = None,
 
     # 2. start barrier: Semaphore start stage (unfenced): one add per rank,
     # wait for W -- or Pattern 0 of the pad barrier.
-    if pad_mode:
+    if cluster:
+        pass
+    elif pad_mode:
         _pad_barrier(st)
     else:
         st.flag = (st.flag + W) & MASK32
@@ -170,7 +178,9 @@ def step(st: State, inputs, skip_end_signal_rank: int | None = None,
 
     # 4. end barrier (fenced): Semaphore end stage -- one add per sending rank,
     # wait for 2W, advance counter -- or Pattern 1 of the pad barrier.
-    if pad_mode:
+    if cluster:
+        pass
+    elif pad_mode:
         _pad_barrier(st, skip_end_signal_rank)
     else:
         senders = W - (1 if skip_end_signal_rank is not None else 0)
@@ -183,8 +193,10 @@ def step(st: State, inputs, skip_end_signal_rank: int | None = None,
     # 5. rank-order reduce of the staged slots.
     out = _reduce([st.slots[par][r] for r in range(W)])
 
-    # 6. exit: zero-resetting pad barrier (Pattern 2), epoch flip, last block out.
-    _pad_barrier(st)
+    # 6. exit: zero-resetting pad barrier (Pattern 2; the cluster barrier in
+    # the cluster reading), epoch flip, last block out.
+    if not cluster:
+        _pad_barrier(st)
     st.epoch = (st.epoch + 1) % 2
     st.blocks[1] = 0
     st.seq = seq

@@ -37,7 +37,8 @@ from test_gpu_reduce import assert_bits_equal
 pytestmark = pytest.mark.gpu
 
 M32 = 0xFFFFFFFF
-SYNCS = ["semaphore", "pad", "pad_fenced"]
+SYNCS = ["semaphore", "pad", "pad_fenced", "cluster"]
+FLAG_SYNCS = SYNCS[:3]          # the variants with in-protocol fault injection
 
 
 @pytest.fixture(scope="module")
@@ -191,7 +192,7 @@ def test_random_small_steps(arx, dev):
         W = int(rng.integers(1, 9))
         n = int(rng.integers(1, 3000))
         B = int(rng.integers(0, 6))
-        sync = SYNCS[int(rng.integers(0, 3))]
+        sync = SYNCS[int(rng.integers(0, len(SYNCS)))]
         slots = "host" if case % 5 == 0 else "one"
         c = Ctx(arx, dev, W, n, B, sync, slots)
         st = model.State(W=W, B=c.B)
@@ -359,7 +360,7 @@ def test_unsigned_wrap_of_seq_and_flags(arx, dev):
     assert w["seq"] == 1
 
 
-@pytest.mark.parametrize("sync,slots", [(m, "one") for m in SYNCS] + [("semaphore", "host")])
+@pytest.mark.parametrize("sync,slots", [(m, "one") for m in FLAG_SYNCS] + [("semaphore", "host")])
 def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
     W, n = 4, 8192
     c = Ctx(arx, dev, W, n, 2, sync, slots)
@@ -456,7 +457,8 @@ def test_switching_sync_modes_between_steps(arx, dev):
     W, n = 6, 30011
     c = Ctx(arx, dev, W, n, 3)
     st = model.State(W=W, B=c.B)
-    for s, sync in enumerate(["semaphore", "pad", "pad_fenced", "semaphore", "pad_fenced", "pad", "semaphore"]):
+    for s, sync in enumerate(["semaphore", "pad", "cluster", "pad_fenced", "semaphore", "cluster", "pad_fenced",
+                              "pad", "cluster", "semaphore"]):
         c.set_sync(sync)
         x = sp.partials(W, n, "normal", seed=300 + s)
         out = _step(arx, c, x, dev)
@@ -481,25 +483,42 @@ def test_mixed_variants_in_one_graph(arx, dev):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for t in range(steps):
-            c.set_sync(SYNCS[t % 3])
+            c.set_sync(SYNCS[t % 4])
             arx.arx_step(c.ctx, [xd[t % 3][r] for r in range(W)], outs[t], stream=s)
     g.replay()
     torch.cuda.synchronize()
     assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, steps, 0)
     got = outs.cpu().view(torch.int16).numpy().view(np.uint16)
     for t in range(steps):
-        assert_bits_equal(got[t], wants[t % 3], f"step {t} ({SYNCS[t % 3]})")
+        assert_bits_equal(got[t], wants[t % 3], f"step {t} ({SYNCS[t % 4]})")
     st = model.State(W=W, B=c.B)
     for t in range(steps):
-        model.step(st, list(sp.to_u16_numpy(xs[t % 3])), sync=SYNCS[t % 3])
+        model.step(st, list(sp.to_u16_numpy(xs[t % 3])), sync=SYNCS[t % 4])
     _compare_to_model(c.words(), st)
 
 
 def test_unknown_sync_mode_is_rejected(arx, dev):
     c = Ctx(arx, dev, 2, 64, 1)
     with pytest.raises(arx.ArxError):
-        arx.arx_ctx_set_sync(c.ctx, 3)
+        arx.arx_ctx_set_sync(c.ctx, 4)
     assert c.ctx.sync_mode == arx.ARX_SYNC_SEMAPHORE
+
+
+def test_cluster_variant_refuses_fault_injection(arx, dev):
+    # The cluster barrier has no flag signal a rank could skip (a block that
+    # never arrived would hold the hardware barrier forever), so the knob is
+    # refused on the host before anything is launched.
+    W, n = 4, 4096
+    c = Ctx(arx, dev, W, n, 2, "cluster")
+    arx.arx_ctx_set_fault(c.ctx, 1)
+    x = sp.partials(W, n, "normal", seed=5)
+    xd = x.to(dev)
+    out = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    assert arx.arx_step(c.ctx, [xd[r] for r in range(W)], out, check=False) == arx.ARX_EINVAL
+    arx.arx_ctx_set_fault(c.ctx, -1)
+    arx.arx_step(c.ctx, [xd[r] for r in range(W)], out)
+    assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, 1, 0)
+    assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))), "cluster")
 
 
 # ---- 10,000 steps in one CUDA graph --------------------------------------------------------

@@ -129,6 +129,26 @@ def test_pad_mode_missing_end_signal_reports_timeout(sync):
     assert st.err == P.ETIMEOUT
 
 
+@pytest.mark.parametrize("W,B,k", [(1, 1, 1), (3, 2, 4), (8, 3, 5)])
+def test_cluster_mode_closed_form(W, B, k):
+    # The single-GPU reading with the W blocks of a chunk in one cluster: the
+    # barriers are the cluster's own, so pad and Semaphores stay untouched
+    # while seq, published, epochs and the slot banks advance as in the others.
+    st = P.State(W=W, B=B)
+    for s in range(k):
+        x = _inputs(W, 32, s)
+        assert np.array_equal(P.step(st, x, sync="cluster"), oracle.reduce(x))
+    assert not st.pad.any() and not st.flag.any() and not st.counter.any()
+    assert (st.epoch == k % 2).all() and st.blocks == [0, 0]
+    assert st.seq == k and st.published == k and st.err == 0
+    assert np.array_equal(st.slots[k & 1][W - 1], _inputs(W, 32, k - 1)[W - 1])
+
+
+def test_cluster_mode_has_no_signal_to_skip():
+    with pytest.raises(ValueError):
+        P.step(P.State(W=2, B=1), _inputs(2, 8, 0), skip_end_signal_rank=0, sync="cluster")
+
+
 def test_unknown_mode_is_rejected():
     with pytest.raises(ValueError):
         P.step(P.State(W=1, B=1), _inputs(1, 8, 0), sync="fenced")
