@@ -279,8 +279,9 @@ int auto_blocks(int W, size_t max_n, arx_status* s) {
   // About one block per SM over the W*B grid for small messages; for large
   // ones about 128 groups of 8 elements staged per block (more loads in
   // flight), up to the resident capacity; at least 32 groups per reducing
-  // block.  Measured on GB300 (W = 8): B = 19 best at 2^17 elements, 38 at
-  // 2^18, the capacity (76) from 2^20 -- 27 % faster than 19 at 2^23.
+  // block.  Measured on GB300 (W = 8, flag barriers): B = 16-19 best at
+  // 2^17 elements, 32-38 at 2^18, the capacity (72-76) from 2^20 -- 27 %
+  // faster than 19 at 2^23.
   size_t B = size_t(sms) / size_t(W);
   const size_t groups = (max_n + 7) / 8;
   const size_t by_size = groups / (size_t(W) * 128);
@@ -289,6 +290,14 @@ int auto_blocks(int W, size_t max_n, arx_status* s) {
   if (B > by_work) B = by_work;
   if (B > size_t(cap / W)) B = size_t(cap / W);
   if (B > ARX_STEP_MAX_BLOCKS) B = ARX_STEP_MAX_BLOCKS;
+  // Latency-bound messages (B up to two blocks per SM over the grid), from
+  // 16 up: a multiple of 8, so the cluster variant's B clusters of W blocks
+  // spread evenly over the GPU's graphics processing clusters (152 SMs in 8
+  // on GB300) -- W = 8 [32, 4096]: 3.56 us per step at 16 against 4.05 at
+  // 19; W = 4: 3.12 at 32 against 3.42 at 38 -- the flag variants within
+  // +-3 %.  At the resident capacity (bandwidth-bound) rounding down cost
+  // 1.5 %, so B stays there.
+  if (B >= 16 && B <= 2 * size_t(sms) / size_t(W)) B &= ~size_t(7);
   if (B < 1) B = 1;
   *s = ARX_OK;
   return int(B);
