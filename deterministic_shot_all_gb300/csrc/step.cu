@@ -34,6 +34,11 @@
 //  * Pad, fenced: as Pad, but all three barriers use acq_rel compare-and-swaps
 //    (the page's "acq_rel" sem everywhere instead of "relaxed" where its
 //    patterns allow it).
+//  * Cluster (no counterpart on the pages, which synchronise separate GPUs):
+//    the W blocks of chunk b are launched as one thread-block cluster and
+//    each barrier is its hardware barrier -- relaxed at start and exit,
+//    release on arrive and acquire on wait after staging.  No flag word takes
+//    part; the launch needs clusters, not cooperative co-residency.
 // One pad serves all three barriers of a step: a send spins until the
 // receiver has consumed the previous signal (the word is back at 0), so
 // consecutive barriers pair their sends and waits in order.
