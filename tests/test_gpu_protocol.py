@@ -206,13 +206,13 @@ def test_random_small_steps(arx, dev):
             _compare_to_model(c.words(), st)
 
 
-def test_two_contexts_step_concurrently_on_two_streams(arx, dev):
-    # Independent contexts share no state: two of them (different W and
-    # barrier variants) run 200 steps each on two streams at once -- two
-    # cooperative grids resident together, each waiting only on its own
-    # blocks -- and every output of both is checked.
+def test_contexts_step_concurrently_on_separate_streams(arx, dev):
+    # Independent contexts share no state: three of them (different W and
+    # barrier variants) run 200 steps each on three streams at once -- two
+    # cooperative grids and one of clusters resident together, each waiting
+    # only on its own blocks -- and every output of all three is checked.
     steps = 200
-    cfg = [(8, 65536, "semaphore"), (3, 40000, "pad")]
+    cfg = [(8, 65536, "semaphore"), (3, 40000, "pad"), (5, 30000, "cluster")]
     ctxs, ins, outs, wants = [], [], [], []
     for W, n, sync in cfg:
         c = Ctx(arx, dev, W, n, 0, sync)
@@ -223,7 +223,7 @@ def test_two_contexts_step_concurrently_on_two_streams(arx, dev):
         outs.append(torch.zeros(steps, n, dtype=torch.bfloat16, device=dev))
         ctxs.append(c)
     torch.cuda.synchronize()
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in cfg]
     for t in range(steps):
         for j, (W, n, sync) in enumerate(cfg):
             xd = ins[j][t % 4]
