@@ -583,7 +583,8 @@ def protocol_graph_point(torch, arx, sp, dev, stream) -> dict:
     every step (a [10000][8][n] device array, 21 GB, far beyond L2), one output
     per step.  The partials are drawn on the device here (timing only; the
     tests check every step bit for bit with the CPU-drawn seeds 4 + step).
-    µs/step = graph replay time / steps."""
+    µs/step = graph replay time / steps; the default barrier variant, and the
+    thread-block cluster barrier under "cluster"."""
     W, n, steps = 8, sp.N_32x4096, sp.GRAPH_STEPS
     inputs = torch.empty(steps, W, n, dtype=torch.bfloat16, device=dev)
     gen = torch.Generator(device=dev).manual_seed(4)
@@ -591,34 +592,44 @@ def protocol_graph_point(torch, arx, sp, dev, stream) -> dict:
         hi = min(steps, lo + 1000)
         inputs[lo:hi] = torch.randn((hi - lo, W, n), generator=gen, device=dev).to(torch.bfloat16)
     outputs = torch.empty(steps, n, dtype=torch.bfloat16, device=dev)
-    ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
-    ctx = arx.arx_ctx_init(ws, W, n)
     lists = [[inputs[t, r] for r in range(W)] for t in range(steps)]
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    t0 = time.perf_counter()
-    with torch.cuda.graph(g, stream=stream):
-        for t in range(steps):
-            arx.arx_step(ctx, lists[t], outputs[t], stream=stream)
-    capture_s = time.perf_counter() - t0
-    times = []
-    with torch.cuda.stream(stream):
-        g.replay()                      # warm-up replay (untimed)
+    res = None
+    # The default barrier variant, then the same graph workload on the
+    # thread-block cluster barrier (reported as "cluster").
+    for sync in (arx.ARX_SYNC_SEMAPHORE, arx.ARX_SYNC_CLUSTER):
+        ws = torch.zeros(arx.arx_ctx_workspace_bytes(W, n), dtype=torch.uint8, device=dev)
+        ctx = arx.arx_ctx_init(ws, W, n)
+        arx.arx_ctx_set_sync(ctx, sync)
         torch.cuda.synchronize()
-        for _ in range(3):
-            s = torch.cuda.Event(enable_timing=True)
-            e = torch.cuda.Event(enable_timing=True)
-            s.record(stream)
-            g.replay()
-            e.record(stream)
+        g = torch.cuda.CUDAGraph()
+        t0 = time.perf_counter()
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(steps):
+                arx.arx_step(ctx, lists[t], outputs[t], stream=stream)
+        capture_s = time.perf_counter() - t0
+        times = []
+        with torch.cuda.stream(stream):
+            g.replay()                      # warm-up replay (untimed)
             torch.cuda.synchronize()
-            times.append(s.elapsed_time(e) / 1e3)
-    st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
-    t = statistics.median(times)
-    res = {"W": W, "n": n, "steps_per_graph": steps, "replays": len(times), "us_per_step": t / steps * 1e6,
-           "graph_ms": t * 1e3, "capture_s": capture_s, "status": arx.arx_status_string(st),
-           "seq": seq, "blocks_per_rank": ctx.nblocks}
-    del g, inputs, outputs, lists
+            for _ in range(3):
+                s = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                g.replay()
+                e.record(stream)
+                torch.cuda.synchronize()
+                times.append(s.elapsed_time(e) / 1e3)
+        st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
+        t = statistics.median(times)
+        point = {"W": W, "n": n, "steps_per_graph": steps, "replays": len(times), "us_per_step": t / steps * 1e6,
+                 "graph_ms": t * 1e3, "capture_s": capture_s, "status": arx.arx_status_string(st),
+                 "seq": seq, "blocks_per_rank": ctx.nblocks}
+        if res is None:
+            res = point
+        else:
+            res["cluster"] = {k: point[k] for k in ("us_per_step", "graph_ms", "status", "seq")}
+        del g, ws
+    del inputs, outputs, lists
     torch.cuda.empty_cache()
     return res
 
