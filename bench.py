@@ -634,7 +634,7 @@ def protocol_graph_point(torch, arx, sp, dev, stream) -> dict:
     return res
 
 
-def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link) -> dict:
+def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link, steps: int = 2000) -> dict:
     """arx_step with the slot banks in page-locked host memory (arx_ctx_init_split):
     every step writes the W staged partials to host memory and reads them back
     over NVLink-C2C.  Link roofline: the time the measured rate of pinned
@@ -654,7 +654,6 @@ def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link) -
     def call(i):
         arx.arx_step(ctx, lists[i % R], outs[i % R], stream=stream)
 
-    steps = 2000
     t = timed_graph_calls(torch, stream, call, steps, 10) / steps
     st, seq, err = arx.arx_ctx_query(ctx, stream=stream)
     moved = W * n * 2
@@ -901,6 +900,22 @@ def run_protocol(args) -> None:
     print(json.dumps({"protocol": res}), flush=True)
 
 
+def run_protocol_host(args) -> None:
+    """Only the protocol step with its slot banks in page-locked host memory
+    (W = 8 bf16 [32, 4096], --steps steps in graphs); prints one JSON object.
+    Used to profile the staggered host-slot step."""
+    import torch
+    import deterministic_shot_all_gb300 as arx
+    import synthetic_partials as sp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2**20)
+    stream = torch.cuda.Stream(device=dev)
+    link = pinned_copy_gbs(torch, dev)
+    res = protocol_host_slots_point(torch, arx, sp, dev, stream, l2, DEFAULT_WORKLOAD, link, steps=args.steps)
+    print(json.dumps({"protocol_host_slots": res, "link": link}), flush=True)
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -919,6 +934,8 @@ def main(argv=None) -> None:
     p.add_argument("--sweep-min", type=int, default=9)
     p.add_argument("--sweep-max", type=int, default=27)
     p.add_argument("--protocol", action="store_true", help="only the protocol step, every barrier variant")
+    p.add_argument("--protocol-host", action="store_true",
+                   help="only the protocol step with its slots in page-locked host memory")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -928,6 +945,8 @@ def main(argv=None) -> None:
         run_sweep(args)
     elif args.protocol:
         run_protocol(args)
+    elif args.protocol_host:
+        run_protocol_host(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
