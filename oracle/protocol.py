@@ -48,6 +48,14 @@ Barrier variants (``sync``), with the same data path:
 * ``"pad_fenced"`` -- as ``"pad"``; only the memory ordering of the start and
   exit barriers differs (acq_rel), which a sequential model does not see, so
   the words after a step are the same as for ``"pad"``.
+* ``"semaphore_global"`` -- the same words as ``"semaphore"``: the two differ
+  only in where a GPU holds the Semaphore flag during the step (global memory,
+  or the shared memory of a thread-block cluster, loaded at entry and written
+  back at exit) and in how the exit waits (the pad barrier above, or the
+  cluster's hardware barrier, which leaves the pad at zero as well).
+  common.cuh's ``PullController::sync`` fixes the arithmetic, not the place.
+* ``"cluster"`` -- the single-GPU reading in which every barrier is a
+  thread-block cluster's hardware barrier: no protocol word takes part.
 
 All protocol words are unsigned 32-bit and wrap modulo 2**32, as the pages'
 ``uint32_t`` flags do (``flag - base`` in ``PullController::sync`` is an
@@ -103,7 +111,7 @@ def _set_err(st: State, code: int) -> None:
         st.err = code
 
 
-SYNC_MODES = ("semaphore", "pad", "pad_fenced", "cluster")
+SYNC_MODES = ("semaphore", "pad", "pad_fenced", "cluster", "semaphore_global")
 
 
 def _pad_barrier(st: State, skip_rank: int | None = None) -> None:
