@@ -16,7 +16,10 @@ Functions keep the C names:
 * ``arx_ctx_workspace_bytes / arx_ctx_init / arx_step / arx_ctx_query /
   arx_ctx_reset / arx_ctx_set_timeout / arx_ctx_set_fault / arx_ctx_set_sync``:
   the seq/parity protocol step with Semaphore epochs and a zero-resetting
-  signal pad, in three barrier variants.
+  signal pad, in five barrier variants.
+* ``arx_ext_*``: the external-writer form -- a host thread writes each
+  rank's partial into page-locked slots and raises its flag, the GPU waits
+  for the flags and reduces.
 """
 
 from __future__ import annotations
@@ -33,7 +36,7 @@ ARX_MAX_W = 8
 ARX_STEP_MAX_BLOCKS = 256
 ARX_DEFAULT_TIMEOUT_NS = 1_000_000_000
 ARX_NOALLOC_MAX_N = 131072
-ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED, ARX_SYNC_CLUSTER = range(4)
+ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED, ARX_SYNC_CLUSTER, ARX_SYNC_SEMAPHORE_GLOBAL = range(5)
 ARX_SLOTS_DEVICE, ARX_SLOTS_HOST = range(2)
 
 
@@ -81,6 +84,25 @@ class arx_ctx(ctypes.Structure):
     ]
 
 
+class arx_ext(ctypes.Structure):
+    """Mirror of ``struct arx_ext`` in include/arx.h."""
+    _fields_ = [
+        ("magic", ctypes.c_uint32),
+        ("W", ctypes.c_int32),
+        ("nblocks", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("max_n", ctypes.c_uint64),
+        ("slot_stride", ctypes.c_uint64),
+        ("timeout_ns", ctypes.c_uint64),
+        ("words", ctypes.c_void_p),
+        ("host_region", ctypes.c_void_p),
+        ("dev_region", ctypes.c_void_p),
+        ("region_bytes", ctypes.c_uint64),
+        ("failed_err", ctypes.c_uint32),
+        ("reserved1", ctypes.c_uint32),
+    ]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -90,6 +112,8 @@ def _load() -> ctypes.CDLL:
     vp, sz, i32, u32p, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_uint64
     ptrs = ctypes.POINTER(ctypes.c_void_p)
     ctxp = ctypes.POINTER(arx_ctx)
+    extp = ctypes.POINTER(arx_ext)
+    u32 = ctypes.c_uint32
     sigs = {
         "arx_status_string": ([i32], ctypes.c_char_p),
         "arx_last_error": ([], ctypes.c_char_p),
@@ -109,6 +133,18 @@ def _load() -> ctypes.CDLL:
         "arx_ctx_query": ([ctxp, u32p, u32p, vp], i32),
         "arx_step_noalloc": ([ptrs, i32, vp, sz, vp, vp], i32),
         "arx_watch_step": ([ctxp, ctypes.c_uint32, u64, u64, u64, u32p, vp, ctypes.POINTER(arx_watch_report)], i32),
+        "arx_ext_region_bytes": ([i32, sz], sz),
+        "arx_ext_words_bytes": ([], sz),
+        "arx_ext_init": ([extp, vp, sz, vp, sz, i32, sz, i32], i32),
+        "arx_ext_set_timeout": ([extp, u64], i32),
+        "arx_ext_wait_free": ([extp, u32, u64], i32),
+        "arx_ext_slot": ([extp, u32, i32], vp),
+        "arx_ext_publish": ([extp, i32, u32], i32),
+        "arx_ext_post": ([extp, i32, u32, vp, sz, u64], i32),
+        "arx_ext_publish_all": ([extp, u32, u64], i32),
+        "arx_ext_step": ([extp, vp, sz, vp], i32),
+        "arx_ext_query": ([extp, u32p, u32p, vp], i32),
+        "arx_ext_reset": ([extp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -358,7 +394,7 @@ def arx_ctx_set_timeout(ctx: arx_ctx, ns: int) -> None:
 
 def arx_ctx_set_sync(ctx: arx_ctx, mode: int) -> None:
     """Barrier variant of later steps: ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD,
-    ARX_SYNC_PAD_FENCED or ARX_SYNC_CLUSTER."""
+    ARX_SYNC_PAD_FENCED, ARX_SYNC_CLUSTER or ARX_SYNC_SEMAPHORE_GLOBAL."""
     _check(lib.arx_ctx_set_sync(ctypes.byref(ctx), int(mode)))
 
 
@@ -450,6 +486,97 @@ def arx_step_noalloc(inputs: Sequence, out, n: int | None = None, dev_status=Non
     return st
 
 
+# ---- external-writer form: a host thread writes the slots, the GPU reduces ----------
+
+def arx_ext_region_bytes(W: int, max_n: int) -> int:
+    return int(lib.arx_ext_region_bytes(W, max_n))
+
+
+def arx_ext_words_bytes() -> int:
+    return int(lib.arx_ext_words_bytes())
+
+
+def arx_ext_init(words, region, W: int, max_n: int, nblocks: int = 0) -> arx_ext:
+    """External-writer context: ``words`` a zero-filled device tensor of
+    ``arx_ext_words_bytes()`` bytes, ``region`` a zero-filled page-locked host
+    tensor (``pin_memory()``) of ``arx_ext_region_bytes(W, max_n)`` bytes."""
+    if not getattr(words, "is_cuda", True):
+        raise ValueError("the device words must be a CUDA tensor")
+    if getattr(region, "is_cuda", False):
+        raise ValueError("the region must be page-locked host memory")
+    x = arx_ext()
+    _check(lib.arx_ext_init(ctypes.byref(x), _ptr(words), words.numel() * words.element_size(),
+                            _ptr(region), region.numel() * region.element_size(), W, max_n, nblocks))
+    x._refs = (words, region)  # keep both buffers alive as long as the context
+    return x
+
+
+def arx_ext_set_timeout(x: arx_ext, ns: int) -> None:
+    _check(lib.arx_ext_set_timeout(ctypes.byref(x), int(ns)))
+
+
+def arx_ext_wait_free(x: arx_ext, seq: int, wait_s: float = 10.0, check: bool = True) -> int:
+    st = lib.arx_ext_wait_free(ctypes.byref(x), int(seq) & 0xFFFFFFFF, int(wait_s * 1e9))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_ext_slot(x: arx_ext, seq: int, rank: int) -> int:
+    """Host address of recv[seq & 1][rank] (raises for bad arguments)."""
+    p = lib.arx_ext_slot(ctypes.byref(x), int(seq) & 0xFFFFFFFF, int(rank))
+    if not p:
+        raise ArxError(ARX_EINVAL, f"no slot for rank {rank}")
+    return int(p)
+
+
+def arx_ext_publish(x: arx_ext, rank: int, seq: int) -> None:
+    _check(lib.arx_ext_publish(ctypes.byref(x), int(rank), int(seq) & 0xFFFFFFFF))
+
+
+def arx_ext_post(x: arx_ext, rank: int, seq: int, src, n: int | None = None, wait_s: float = 10.0,
+                 check: bool = True) -> int:
+    """Producer: wait until bank ``seq & 1`` is free, copy ``src`` (a host bf16
+    tensor or address of n elements) into recv[seq & 1][rank], raise flag[rank]."""
+    if n is None:
+        n = int(src.numel())
+    if not isinstance(src, int):
+        _check_bf16([src], n, "cpu", "src")
+    st = lib.arx_ext_post(ctypes.byref(x), int(rank), int(seq) & 0xFFFFFFFF, _ptr(src), n, int(wait_s * 1e9))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_ext_publish_all(x: arx_ext, seq: int, wait_s: float = 10.0, check: bool = True) -> int:
+    st = lib.arx_ext_publish_all(ctypes.byref(x), int(seq) & 0xFFFFFFFF, int(wait_s * 1e9))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_ext_step(x: arx_ext, out, n: int | None = None, stream=None, check: bool = True) -> int:
+    """Consumer: enqueue the next step, out = rank-order reduce of the posted slots."""
+    n = _numel(n, out)
+    if not isinstance(out, int):
+        _check_bf16([out], n, "cuda", "out")
+    st = lib.arx_ext_step(ctypes.byref(x), _ptr(out), n, _stream(stream))
+    if check:
+        _check(st)
+    return st
+
+
+def arx_ext_query(x: arx_ext, stream=None) -> tuple[int, int, int]:
+    seq = ctypes.c_uint32(0)
+    err = ctypes.c_uint32(0)
+    st = lib.arx_ext_query(ctypes.byref(x), ctypes.byref(seq), ctypes.byref(err), _stream(stream))
+    return st, seq.value, err.value
+
+
+def arx_ext_reset(x: arx_ext, stream=None) -> None:
+    _check(lib.arx_ext_reset(ctypes.byref(x), _stream(stream)))
+
+
 __all__ = [
     "ArxError", "arx_ctx", "lib", "arx_status_string", "arx_last_error", "arx_reduce", "arx_reduce_plan",
     "arx_step_plan",
@@ -457,4 +584,7 @@ __all__ = [
     "arx_ctx_words_bytes", "arx_ctx_slots_bytes", "arx_ctx_init_split",
     "arx_ctx_set_timeout", "arx_ctx_set_fault", "arx_ctx_set_sync", "arx_ctx_reset", "arx_step", "arx_ctx_query",
     "arx_step_noalloc", "arx_watch_step", "arx_watch_report",
+    "arx_ext", "arx_ext_region_bytes", "arx_ext_words_bytes", "arx_ext_init", "arx_ext_set_timeout",
+    "arx_ext_wait_free", "arx_ext_slot", "arx_ext_publish", "arx_ext_post", "arx_ext_publish_all",
+    "arx_ext_step", "arx_ext_query", "arx_ext_reset",
 ]

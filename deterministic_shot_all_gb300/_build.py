@@ -29,7 +29,7 @@ LIB = os.path.join(PKG, "libarx.so")
 CHECK_OBJ_DIR = os.path.join(PKG, "_build_boundscheck")
 CHECK_LIB = os.path.join(PKG, "libarx_boundscheck.so")
 
-SOURCES = ["reduce.cu", "step.cu", "abi.cu", "step_noalloc.cu"]
+SOURCES = ["reduce.cu", "step.cu", "abi.cu", "step_noalloc.cu", "external.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("arx_device.cuh", "arx_internal.h")] + [
     os.path.join(INCLUDE, "arx.h")]
 

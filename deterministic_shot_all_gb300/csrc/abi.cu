@@ -5,7 +5,6 @@
 // and drops its 512 KB / multiple-of-8 limits.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
@@ -81,9 +80,6 @@ namespace {
 // their buffer (one counter per device, in this library's device image).
 __device__ uint32_t g_bounds_violations;
 
-constexpr int kMaxCounterDevices = 64;
-std::atomic<uint32_t*> g_counter_address[kMaxCounterDevices];
-
 __global__ void bounds_probe_kernel(uint32_t* counter, const uint16_t* base) {
   // One address past the end of an 8-element buffer: counted, never accessed.
   ARX_CHECKED(base + 8, 2, base, 16, counter, atomicAdd(counter, uint32_t(base[8])));
@@ -95,20 +91,12 @@ __global__ void bounds_probe_kernel(uint32_t* counter, const uint16_t* base) {
 namespace arx {
 
 #ifdef ARX_BOUNDS_CHECK
+// Looked up on every call, not cached: after cudaDeviceReset the context is
+// created again and the counter has a new address.
 uint32_t* bounds_counter(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= kMaxCounterDevices) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  uint32_t* p = g_counter_address[dev].load();
-  if (p) return p;
   void* q = nullptr;
   *err = cudaGetSymbolAddress(&q, g_bounds_violations);
   if (*err != cudaSuccess || !q) return nullptr;
-  g_counter_address[dev].store(static_cast<uint32_t*>(q));
   return static_cast<uint32_t*>(q);
 }
 #endif
@@ -289,6 +277,15 @@ int auto_blocks(int W, size_t max_n, arx_status* s) {
   const size_t by_work = (groups + size_t(W) * 32 - 1) / (size_t(W) * 32);
   if (B > by_work) B = by_work;
   if (B > size_t(cap / W)) B = size_t(cap / W);
+  // The cluster-launched variants (one cluster of W blocks per chunk) run in
+  // one wave only if every cluster is resident at once; clusters stay within
+  // one GPU processing cluster, so that can be fewer than cap / W.
+  const int ccap = arx::step_cluster_capacity(W, &e);
+  if (ccap < 1) {
+    *s = fail_cuda(e, "arx_ctx_init cluster occupancy query");
+    return -1;
+  }
+  if (B > size_t(ccap)) B = size_t(ccap);
   if (B > ARX_STEP_MAX_BLOCKS) B = ARX_STEP_MAX_BLOCKS;
   // Latency-bound messages (B up to two blocks per SM over the grid), from
   // 16 up: a multiple of 8, so the cluster variant's B clusters of W blocks
@@ -431,7 +428,7 @@ arx_status arx_ctx_set_sync(arx_ctx* ctx, int mode) {
   const arx_status s = check_ctx(ctx);
   if (s != ARX_OK) return s;
   if (mode != ARX_SYNC_SEMAPHORE && mode != ARX_SYNC_PAD && mode != ARX_SYNC_PAD_FENCED &&
-      mode != ARX_SYNC_CLUSTER)
+      mode != ARX_SYNC_CLUSTER && mode != ARX_SYNC_SEMAPHORE_GLOBAL)
     return fail(ARX_EINVAL, "unknown sync mode %d", mode);
   ctx->sync_mode = mode;
   return ok();
@@ -463,7 +460,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   if (n == 0) return ok();
   if (n > ctx->max_n) return fail(ARX_EINVAL, "n=%zu exceeds the context's max_n=%llu", n,
                                   static_cast<unsigned long long>(ctx->max_n));
-  if (ctx->sync_mode < ARX_SYNC_SEMAPHORE || ctx->sync_mode > ARX_SYNC_CLUSTER)
+  if (ctx->sync_mode < ARX_SYNC_SEMAPHORE || ctx->sync_mode > ARX_SYNC_SEMAPHORE_GLOBAL)
     return fail(ARX_ESTATE, "context holds an unknown sync mode %d", ctx->sync_mode);
   if (ctx->sync_mode == ARX_SYNC_CLUSTER && ctx->fault_rank >= 0)
     return fail(ARX_EINVAL, "fault injection skips a flag signal; the cluster barrier has none to skip");

@@ -205,6 +205,56 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ---- distributed shared memory (words in another block of the cluster) ---------
+
+// Shared-window address of a __shared__ variable of this block.
+__device__ __forceinline__ uint32_t shared_address(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// The same variable in the block of cluster rank `rank`, as a shared::cluster
+// address.
+__device__ __forceinline__ uint32_t cluster_peer_address(uint32_t shared_addr, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(shared_addr), "r"(rank));
+  return a;
+}
+
+// Fire-and-forget adds to a word in a cluster peer's shared memory: relaxed,
+// or release at cluster scope (the issuing thread's earlier writes, global
+// ones included, are visible to the cluster before the add is).
+__device__ __forceinline__ void red_add_relaxed_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_release_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("red.release.cluster.shared::cluster.add.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Loads of a word in this block's own shared memory that cluster peers add
+// to: relaxed, or acquire at cluster scope.
+__device__ __forceinline__ uint32_t ld_relaxed_cluster_shared(uint32_t shared_addr) {
+  uint32_t v;
+  asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(shared_addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_cluster_shared(uint32_t shared_addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(shared_addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_shared(uint32_t shared_addr, uint32_t v) {
+  asm volatile("st.shared::cta.u32 [%0], %1;" :: "r"(shared_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 // ---- scoped atomics and loads for the protocol words (one GPU: .gpu scope) -------
 
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
@@ -245,6 +295,42 @@ __device__ __forceinline__ uint32_t atom_cas_acquire_gpu(uint32_t* p, uint32_t c
   uint32_t old;
   asm volatile("atom.acquire.gpu.global.cas.b32 %0, [%1], %2, %3;"
                : "=r"(old) : "l"(p), "r"(cmp), "r"(val) : "memory");
+  return old;
+}
+
+// ---- words and data another agent (a host thread) writes: system scope ----------
+
+// Acquire at system scope: the writes the writer released before storing the
+// word are visible to this thread's later loads.
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_sys(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.sys.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Cache-bypassing loads ("fetch again"): a cached copy of a host-memory line
+// is treated as stale and read anew, so data another agent rewrote is never
+// served from an earlier step's line.
+__device__ __forceinline__ uint4 ld_cv(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.cv.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_cv16(const uint16_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.cv.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
 

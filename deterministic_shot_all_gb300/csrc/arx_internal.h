@@ -57,6 +57,10 @@ cudaError_t launch_step(const StepCall& c, cudaStream_t stream);
 // the current device (SMs x blocks per SM), or a negative value on error.
 int step_capacity(int W, cudaError_t* err);
 
+// Most clusters of (1, W, 1) step blocks that can be resident at once on the
+// current device (the cluster-launched variants), or a negative value on error.
+int step_cluster_capacity(int W, cudaError_t* err);
+
 // SM count of the current device (cached per device ordinal).
 int current_sm_count(cudaError_t* err);
 

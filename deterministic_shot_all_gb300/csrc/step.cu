@@ -25,7 +25,21 @@
 //     completed (arx.cu "last block out").
 //
 // Barrier variants (the context's sync mode), all with the same data path:
-//  * Semaphore (default): steps 2 and 4 as above, step 6 a relaxed pad barrier.
+//  * Semaphore (default): steps 2 and 4 as above, with each block's flag held
+//    for the step in its shared memory.  The W blocks of chunk b are one
+//    thread-block cluster; they add to each other's flags through
+//    distributed shared memory and the owner polls its own.  The flag and
+//    counter are loaded at entry and written back at exit, so the words in
+//    memory follow the same arithmetic.  The cluster barrier runs in two
+//    split phases: arrive after zeroing the shared flag, wait before the
+//    first remote add (every flag is in place); arrive after the last remote
+//    add, wait just before exit (no add reaches an exited block).  Step 6 is
+//    that last wait: it also tells every block of the chunk that all reads of
+//    the chunk's slots are done, which is the pad barrier's Pattern 2.
+//  * Semaphore, global: steps 2 and 4 with the flags in the workspace (as the
+//    page keeps them for peers on other GPUs), step 6 a relaxed pad barrier.
+//    Also used for host-slot steps that stage in turn (their waits cross
+//    clusters).
 //  * Pad: every barrier is triton_barrier.py's `blockwise_barrier` on the
 //    signal pad, in the page's three patterns -- Pattern 0 at the start
 //    (relaxed barrier, then block sync), Pattern 1 after staging (block sync,
@@ -43,10 +57,14 @@
 // receiver has consumed the previous signal (the word is back at 0), so
 // consecutive barriers pair their sends and waits in order.
 //
-// Every wait is bounded by the context's timeout (global timer plus a spin
-// cap): on expiry the block records ARX_ETIMEOUT with its stage, rank and
-// block in the error word and carries on, so the kernel always finishes and
-// the host reads the status.  The pages' waits are unbounded; these are not.
+// Every flag wait is bounded by the context's timeout (global timer plus a
+// spin cap): on expiry the block records ARX_ETIMEOUT with its stage, rank
+// and block in the error word and carries on, so the kernel always finishes
+// and the host reads the status.  The pages' waits are unbounded; these are
+// not.  The cluster barrier's wait is a hardware wait without a timeout: it
+// completes because every thread of every block arrives unconditionally.
+// Code in the cluster variants must never return early or arrive
+// conditionally (the fault knob skips a flag add, never an arrival).
 //
 // Latency choices (measured on GB300, W = 8, bf16 [32, 4096]): the kernel is
 // a programmatic dependent of the previous kernel on its stream (it waits for
@@ -81,7 +99,9 @@ enum Stage : uint32_t {
 };
 
 // Barrier variants (arx.h, ARX_SYNC_*).
-enum SyncMode : int { kSyncSemaphore = 0, kSyncPad = 1, kSyncPadFenced = 2, kSyncCluster = 3 };
+enum SyncMode : int {
+  kSyncSemaphore = 0, kSyncPad = 1, kSyncPadFenced = 2, kSyncCluster = 3, kSyncSemaphoreGlobal = 4
+};
 
 // 16-byte vectors each thread loads before storing them while staging.
 constexpr int kStageBatch = 4;
@@ -165,6 +185,25 @@ __device__ bool semaphore_wait(const uint32_t* flag, uint32_t base, uint32_t tar
   }
 }
 
+// The same wait on a Semaphore flag in this block's own shared memory, which
+// the blocks of its cluster add to: polls with relaxed cluster-scope loads;
+// kAcquire (end stage) makes the successful poll an acquire at cluster scope,
+// so the peers' staged writes released before their adds are visible.
+template <bool kAcquire>
+__device__ bool shared_semaphore_wait(uint32_t flag_addr, uint32_t base, uint32_t target,
+                                      uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  const uint64_t cap = spin_cap(timeout_ns);
+  for (uint64_t spins = 0;; ++spins) {
+    const uint32_t v = kAcquire ? ld_acquire_cluster_shared(flag_addr) : ld_relaxed_cluster_shared(flag_addr);
+    if (v - base >= target) return true;
+    if ((spins & 15u) == 15u) {
+      if (global_timer_ns() - t0 > timeout_ns || spins > cap) return false;
+      backoff(spins);
+    }
+  }
+}
+
 // Wait until a count (zero before the step) has reached `target`, bounded.
 __device__ bool count_wait(const uint32_t* count, uint32_t target, uint64_t timeout_ns) {
   return semaphore_wait<false>(count, 0u, target, timeout_ns);
@@ -237,7 +276,10 @@ template <int W, int kSync, bool kStagger>
 __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   constexpr bool kPad = kSync == kSyncPad || kSync == kSyncPadFenced;
   constexpr bool kCluster = kSync == kSyncCluster;  // grid clusters of (1, W, 1)
+  constexpr bool kDsm = kSync == kSyncSemaphore;    // clusters too; Semaphores in shared memory
+  constexpr bool kSemGlobal = kSync == kSyncSemaphoreGlobal;
   constexpr bool kFencedAll = kSync == kSyncPadFenced;
+  static_assert(!(kStagger && (kCluster || kDsm)), "staggered staging waits across clusters");
   const uint32_t b = blockIdx.x, r = blockIdx.y;
   const uint32_t B = uint32_t(a.B);
   const uint32_t tid = threadIdx.x, warp = tid / 32u, lane = tid % 32u;
@@ -250,6 +292,13 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 
   __shared__ uint32_t s_seq;
   __shared__ uint32_t s_epoch;
+  // Semaphore variant: this block's Semaphore flag (common.cuh `Semaphore`),
+  // held in its shared memory for the step; the W blocks of the cluster add
+  // to it through distributed shared memory.  The counter is read and
+  // written only by its owner, so it stays in a register (`base`).
+  __shared__ uint32_t s_sem_flag;
+  const uint32_t flag_sh = shared_address(&s_sem_flag);
+  const uint32_t owner = 32u * r;  // warp r, lane 0: the thread that waits on this block's flag
 
   // Chunk b (in 16-byte groups) of rank r's input.
   const size_t G = a.n / 8u;
@@ -276,6 +325,26 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     s_epoch = epoch_in;
     if (epoch_in != ((seq - 1u) & 1u)) record_error(&hdr->err, kErrState, kEpoch, r, b);
   }
+  Semaphore& own = sem[r * B + b];
+  uint32_t base = 0;
+  uint32_t flag_in = 0;  // Semaphore variant: the flag as the previous step left it
+  if constexpr (kDsm) {
+    // The shared word counts this step's adds from zero; the owner keeps the
+    // flag and counter of the previous step in registers, so the words obey
+    // the page's arithmetic -- flag - counter = (flag_in + adds) - counter,
+    // i.e. adds - base with base = counter - flag_in.  Zero the word and
+    // arrive at the cluster barrier at once (release: the zero is visible to
+    // the cluster before any peer's add can reach it); the global words are
+    // loaded after the arrival, so their latency overlaps the barrier.  The
+    // wait comes after the first staging loads below.
+    if (tid == owner) st_shared(flag_sh, 0u);
+    __syncwarp();  // the cluster barrier instructions are warp-aligned
+    cluster_arrive_release();
+    if (tid == owner) {
+      flag_in = own.flag;
+      base = own.counter - flag_in;
+    }
+  }
 
   // The first batch of this block's staging loads.  They read only the
   // caller's input, which no barrier guards, so they are issued before the
@@ -291,13 +360,23 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   }
 
   // 2. start barrier.
-  Semaphore& own = sem[r * B + b];
-  uint32_t base = 0;
-  if constexpr (kCluster) {
+  if constexpr (kDsm) {
+    // PullController start stage, unfenced, on the shared-memory flags: once
+    // every block of the cluster has its flag in place (the hardware
+    // barrier), lane 0 of warp q < W adds 1 to block q's flag; lane 0 of
+    // warp r waits for W.
+    __syncwarp();
+    cluster_wait();
+    if (lane == 0 && warp < uint32_t(W)) {
+      red_add_relaxed_cluster(cluster_peer_address(flag_sh, warp), 1u);
+      if (warp == r && !shared_semaphore_wait<false>(flag_sh, base, uint32_t(W), a.timeout_ns))
+        record_error(&hdr->err, kErrTimeout, kStartWait, r, b);
+    }
+  } else if constexpr (kCluster) {
     // The W blocks of chunk b are one cluster: its hardware barrier, relaxed.
     cluster_arrive_relaxed();
     cluster_wait();
-  } else if constexpr (!kPad) {
+  } else if constexpr (kSemGlobal) {
     // PullController start stage, unfenced: no block barrier before the signal.
     if (lane == 0 && warp < uint32_t(W)) {
       red_add_relaxed_gpu(&sem[warp * B + b].flag, 1u);
@@ -408,6 +487,30 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
         st_relaxed_gpu(&hdr->published, seq);
       }
     }
+  } else if constexpr (kDsm) {
+    // PullController end stage on the shared-memory flags: release adds at
+    // cluster scope (after the block barrier: the whole block's staging),
+    // then the cluster barrier's second arrival -- every write this block
+    // makes to a peer's shared memory is issued before it, so once all have
+    // arrived no block still writes into another (the wait is at exit).
+    // Lane 0 of warp r waits for 2W with acquire and advances the counter.
+    if (lane == 0 && warp < uint32_t(W) && int(r) != a.fault_rank)
+      red_add_release_cluster(cluster_peer_address(flag_sh, warp), 1u);
+    __syncwarp();
+    cluster_arrive_release();
+    if (tid == owner) {
+      if (shared_semaphore_wait<true>(flag_sh, base, 2u * uint32_t(W), a.timeout_ns)) {
+        base += 2u * uint32_t(W);  // the counter after this step
+      } else {
+        record_error(&hdr->err, kErrTimeout, kEndWait, r, b);
+      }
+    } else if (tid == 1) {
+      // Last block past the copy publishes seq (only the host watchdog reads it).
+      if (atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
+        hdr->blocks[0] = 0u;
+        st_relaxed_gpu(&hdr->published, seq);
+      }
+    }
   } else if (lane == 0 && warp < uint32_t(W)) {
     if (int(r) != a.fault_rank) {
       // Release after the block barrier: every thread's staged data is
@@ -484,7 +587,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // [32, 4096], A/B of two builds in one process, the same on two GPUs).
   __syncthreads();
   if constexpr (kCluster) cluster_arrive_relaxed();
-  if (!kCluster && tid < uint32_t(W)) {
+  if ((kPad || kSemGlobal) && tid < uint32_t(W)) {
     pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
                             kPadWait);
   } else if (tid == 32u) {
@@ -503,9 +606,22 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       st_relaxed_gpu(&hdr->seq, seq);
     }
   }
-  if constexpr (kCluster) {
+  if constexpr (kCluster || kDsm) {
+    // Every block of the cluster passes this wait before it exits: in the
+    // Semaphore variant no peer can then still be adding to this block's
+    // shared memory.  All arrivals are unconditional (no thread returns
+    // early, and the fault knob only skips an add), so the wait always ends.
     __syncwarp();
     cluster_wait();
+  }
+  if constexpr (kDsm) {
+    // Write the step's Semaphore words back (common.cuh keeps them in memory
+    // between calls): the flag with every add of the step counted, the
+    // counter advanced by 2W after a successful end stage.
+    if (tid == owner) {
+      own.flag = flag_in + ld_relaxed_cluster_shared(flag_sh);
+      own.counter = base + flag_in;
+    }
   }
 }
 
@@ -522,11 +638,12 @@ int blocks_per_sm(int dev, cudaError_t* err) {
     if (c > 0) return c;
   }
   int lo = 0;
-  const void* kernels[7] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+  const void* kernels[8] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, true>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphoreGlobal, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphoreGlobal, true>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, true>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, true>)};
   for (const void* k : kernels) {
@@ -582,10 +699,29 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   cfg.numAttrs = 2;
   cudaError_t err = cudaErrorInvalidValue;
   const bool st = a.stagger >= 2u;
+  // The W blocks of a chunk as one cluster of (1, W, 1), waiting only on each
+  // other: clusters need not be resident together, so no cooperative launch.
+  cudaLaunchAttribute cattr[2];
+  cattr[0].id = cudaLaunchAttributeClusterDimension;
+  cattr[0].val.clusterDim.x = 1;
+  cattr[0].val.clusterDim.y = unsigned(W);
+  cattr[0].val.clusterDim.z = 1;
+  cattr[1] = attr[1];
   switch (c.sync_mode) {
     case kSyncSemaphore:
-      err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore, true>, a)
-               : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore, false>, a);
+      if (st) {
+        // Staggered staging (slots in host memory) waits across clusters, so
+        // the Semaphores stay in global memory and the grid is cooperative.
+        err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphoreGlobal, true>, a);
+      } else {
+        cfg.attrs = cattr;
+        cfg.numAttrs = 2;
+        err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore, false>, a);
+      }
+      break;
+    case kSyncSemaphoreGlobal:
+      err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphoreGlobal, true>, a)
+               : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphoreGlobal, false>, a);
       break;
     case kSyncPad:
       err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPad, true>, a)
@@ -595,25 +731,52 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
       err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPadFenced, true>, a)
                : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPadFenced, false>, a);
       break;
-    case kSyncCluster: {
-      // The W blocks of a chunk form one cluster and wait only on each
-      // other (no staggered staging in this variant): clusters need not be
-      // resident together, so no cooperative launch.
-      cudaLaunchAttribute cattr[2];
-      cattr[0].id = cudaLaunchAttributeClusterDimension;
-      cattr[0].val.clusterDim.x = 1;
-      cattr[0].val.clusterDim.y = unsigned(W);
-      cattr[0].val.clusterDim.z = 1;
-      cattr[1] = attr[1];
+    case kSyncCluster:
+      // No staggered staging in this variant (arx_step passes none).
       cfg.attrs = cattr;
       cfg.numAttrs = 2;
       err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncCluster, false>, a);
       break;
-    }
     default: break;
   }
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+// Clusters of (1, W, 1) blocks of the cluster-launched step kernels that can
+// be resident at once on the current device: the least over those kernels.
+// A cluster's blocks share one GPU processing cluster, so this can be fewer
+// than the resident blocks / W (GB300: 152 SMs in 8 of them).
+template <int W>
+int cluster_capacity_w(cudaError_t* err) {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(1, unsigned(W), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = unsigned(W);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int lo = 0;
+  const void* kernels[2] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>)};
+  for (const void* k : kernels) {
+    int c = 0;
+    *err = cudaOccupancyMaxActiveClusters(&c, k, &cfg);
+    if (*err != cudaSuccess || c < 1) return -1;
+    lo = lo == 0 || c < lo ? c : lo;
+  }
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(lo, std::memory_order_relaxed);
+  return lo;
 }
 
 template <int W>
@@ -640,6 +803,20 @@ cudaError_t launch_step(const StepCall& c, cudaStream_t stream) {
     case 7: return launch_w<7>(c, stream);
     case 8: return launch_w<8>(c, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int step_cluster_capacity(int W, cudaError_t* err) {
+  switch (W) {
+    case 1: return cluster_capacity_w<1>(err);
+    case 2: return cluster_capacity_w<2>(err);
+    case 3: return cluster_capacity_w<3>(err);
+    case 4: return cluster_capacity_w<4>(err);
+    case 5: return cluster_capacity_w<5>(err);
+    case 6: return cluster_capacity_w<6>(err);
+    case 7: return cluster_capacity_w<7>(err);
+    case 8: return cluster_capacity_w<8>(err);
+    default: *err = cudaErrorInvalidValue; return -1;
   }
 }
 

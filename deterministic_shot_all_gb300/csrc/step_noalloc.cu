@@ -16,8 +16,6 @@
 // the array and must not be issued.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "arx.h"
 #include "arx_internal.h"
 
@@ -40,35 +38,20 @@ constexpr size_t kScratchBytes = kOffSlots + 2 * size_t(ARX_MAX_W) * kSlotStride
 // the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void* g_scratch_address[kMaxDevices];
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of the scratch in the current device's current context.
+// Looked up on every call rather than cached: a context torn down by
+// cudaDeviceReset and created again reloads this library's device code at a
+// new address, and a cached one would then point at freed memory.  After the
+// first call in a context the lookup is a table search in the runtime.
 void* scratch_address(arx_status* st) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    *st = arx::report(ARX_ECUDA, "arx_step_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    *st = arx::report(ARX_ECUDA, "arx_step_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
     return nullptr;
-  }
-  if (dev < 0 || dev >= kMaxDevices) {
-    *st = arx::report(ARX_EINVAL, "arx_step_noalloc: device ordinal %d beyond %d", dev, kMaxDevices);
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_address[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      *st = arx::report(ARX_ECUDA, "arx_step_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      return nullptr;
-    }
-    g_scratch_address[dev] = p;
   }
   *st = ARX_OK;
-  return g_scratch_address[dev];
+  return p;
 }
 
 }  // namespace

@@ -140,9 +140,12 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  *   5. reduce sub-range r of chunk b over slots[par][0..W-1] into out;
  *   6. pad barrier (0->1 sends, 1->0 waits), epoch[r][b] ^= 1, last block out
  *      stores seq as completed.
- * The output equals arx_reduce's bit for bit.  Every wait is bounded by the
- * context's timeout; on expiry the block records ARX_ETIMEOUT in the device
- * error word and carries on, so the kernel always finishes.
+ * The output equals arx_reduce's bit for bit.  Every flag wait is bounded by
+ * the context's timeout; on expiry the block records ARX_ETIMEOUT in the
+ * device error word and carries on, so the kernel always finishes (the
+ * cluster barriers of ARX_SYNC_SEMAPHORE and ARX_SYNC_CLUSTER are hardware
+ * waits that complete because every thread arrives unconditionally; see the
+ * barrier variants below).
  *
  * Workspace: one caller-owned device buffer, ZERO-FILLED before the first
  * step (e.g. torch.zeros(uint8)), of arx_ctx_workspace_bytes(W, max_n,
@@ -233,11 +236,33 @@ arx_status arx_ctx_init_split(arx_ctx* ctx, void* words, size_t words_bytes, voi
 arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
 
 /* Barrier variants of the step (same data path and result; they differ in
- * which of the pages' barriers run and in their memory ordering):
- *  ARX_SYNC_SEMAPHORE   common.cuh's PullController over the Semaphores for
- *                       the start (unfenced) and end (fenced: release adds,
- *                       acquire waits) barriers; triton_barrier.py's
- *                       blockwise_barrier, Pattern 2, relaxed, at exit.
+ * which of the pages' barriers run, where their words live and in their
+ * memory ordering):
+ *  ARX_SYNC_SEMAPHORE   (default) common.cuh's PullController over the
+ *                       Semaphores for the start (unfenced) and end (release
+ *                       adds, acquire waits) barriers, with each Semaphore
+ *                       flag held for the step in its block's shared memory:
+ *                       the W blocks of a chunk are one thread-block cluster
+ *                       and add to each other's flags through distributed
+ *                       shared memory.  The flag and counter are loaded from
+ *                       the workspace at entry and written back at exit, so
+ *                       the words follow the same arithmetic as in the
+ *                       global form.  The cluster's hardware barrier runs
+ *                       twice, split into arrive and wait (between them the
+ *                       block stages, or reduces): once so that every flag is
+ *                       loaded before a peer adds to it, and once before exit
+ *                       so that no peer still adds to an exited block.  Both
+ *                       complete whatever the flags do (every thread arrives
+ *                       unconditionally), and every flag wait is bounded, so
+ *                       the fault knob works as in the flag modes below.
+ *                       Steps with slots in host memory that stage in turn
+ *                       (see arx_ctx_init_split) wait across chunks and run
+ *                       in the global form (ARX_SYNC_SEMAPHORE_GLOBAL).
+ *  ARX_SYNC_SEMAPHORE_GLOBAL  the same barriers with the Semaphores in the
+ *                       workspace (global memory), as the page keeps them for
+ *                       peers on other GPUs; triton_barrier.py's
+ *                       blockwise_barrier, Pattern 2, relaxed, at exit; a
+ *                       cooperative grid.
  *  ARX_SYNC_PAD         triton_barrier.py's blockwise_barrier on the signal
  *                       pad for all three: Pattern 0 (relaxed) at the start,
  *                       Pattern 1 (acq_rel) after staging, Pattern 2
@@ -251,14 +276,23 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
  *                       and exit; release on arrive, acquire on wait after
  *                       staging).  Semaphores and pad are left alone; seq,
  *                       epochs and the counters advance as in the others.
- *                       The fault-injection knob is refused (ARX_EINVAL) and
- *                       slots in host memory are staged all at once.
+ *                       The hardware barrier's wait has no timeout: it cannot
+ *                       stall because every thread arrives unconditionally,
+ *                       and the fault-injection knob, which would make a
+ *                       block skip an arrival, is refused (ARX_EINVAL).  So
+ *                       "every wait is bounded" holds in this mode only in
+ *                       that sense.  Slots in host memory are staged all at
+ *                       once.
  * After every completed step the pad is all zero in every mode; in the pad
- * and cluster modes the Semaphore flags and counters keep their values. */
+ * and cluster modes the Semaphore flags and counters keep their values.
+ * Every mode may be selected on any context: the co-residency limit that
+ * arx_step checks (B * W blocks resident at once) applies in all of them,
+ * because the cooperative modes need it and a context may switch modes. */
 #define ARX_SYNC_SEMAPHORE 0
 #define ARX_SYNC_PAD 1
 #define ARX_SYNC_PAD_FENCED 2
 #define ARX_SYNC_CLUSTER 3
+#define ARX_SYNC_SEMAPHORE_GLOBAL 4
 
 /* Selects the barrier variant of later steps (ARX_EINVAL for an unknown
  * mode).  Switching between steps is allowed: every mode leaves the pad all
@@ -341,6 +375,114 @@ arx_status arx_watch_step(const arx_ctx* ctx, uint32_t target_seq, uint64_t stal
                           void* stream, arx_watch_report* report);
 
 /* ---------------------------------------------------------------------------
+ * External-writer form: partials written into page-locked host memory by
+ * another agent (a host thread), reduced by the GPU.
+ *
+ * arx.cu's GB10 design: for step seq a CPU proxy has every peer's partial
+ * written into pinned recv[seq & 1][rank] and then raises flag[rank]; the
+ * kernel waits for the flags with system-scope acquire loads and reads the
+ * slots with cache-bypassing loads ("the NIC wrote it"), then sums them in
+ * rank order (header comment, steps 1-3; `arx_kernel`, wait phase and reduce
+ * loop).  On one GB300 the writer is a host thread standing in for the proxy
+ * and the NIC:
+ *   producer (host):  arx_ext_post(x, r, seq, src, n) for r = 0..W-1 --
+ *                     waits until bank seq & 1 is free (the GPU has consumed
+ *                     step seq - 2), copies src into recv[seq & 1][r], then
+ *                     release-stores flag[r] = seq;
+ *   consumer (GPU):   arx_ext_step(x, out, n, stream) -- step seq = completed
+ *                     + 1 waits until every flag[r] has reached seq (bounded
+ *                     ld.acquire.sys polls), writes out = the rank-order
+ *                     reduce of recv[seq & 1][0..W-1] (ld.global.cv loads),
+ *                     and its last block stores seq as completed and, with a
+ *                     system-scope release, as `consumed`.
+ * Steps are numbered 1, 2, 3, ... from a zero-filled (or reset) context; the
+ * producer may run up to two steps ahead of the GPU (the two banks).
+ *
+ * Host region: page-locked host memory (cudaHostAlloc, cudaHostRegister,
+ * torch pin_memory), 256-byte aligned, zero-filled before the first step, of
+ * arx_ext_region_bytes(W, max_n) bytes:
+ *   [0, 512)     uint32 flag[r] at byte 64 * r (written by the producer)
+ *   [512, 516)   uint32 consumed (written by the GPU)
+ *   [1024, ...)  bf16 recv[2][W][slot_stride], slot_stride = max_n rounded up
+ *                to 128 elements; arx_ext_slot gives a slot's host address
+ * Device words: a zero-filled device buffer of arx_ext_words_bytes() bytes,
+ * 256-byte aligned: uint32 completed seq, device error word (stage 11: a
+ * flag wait expired; rank in bits 12-15, block in bits 16-31), blocks out.
+ * Both buffers are the caller's and must outlive the last step.
+ * ------------------------------------------------------------------------- */
+typedef struct arx_ext {
+  uint32_t magic;        /* set by arx_ext_init */
+  int32_t W;             /* writers (virtual ranks), 1..ARX_MAX_W */
+  int32_t nblocks;       /* thread blocks of a step (at most) */
+  int32_t reserved0;
+  uint64_t max_n;        /* capacity of one slot, elements */
+  uint64_t slot_stride;  /* elements from one slot to the next (multiple of 128) */
+  uint64_t timeout_ns;   /* bound of the GPU's flag waits */
+  void* words;           /* device words */
+  void* host_region;     /* host address of the page-locked region */
+  void* dev_region;      /* its device address */
+  uint64_t region_bytes;
+  uint32_t failed_err;   /* nonzero device error word read by arx_ext_query:
+                            arx_ext_step refuses (ARX_ESTATE) until arx_ext_reset */
+  uint32_t reserved1;
+} arx_ext;
+
+/* Bytes of the host region for W writers and slots of max_n elements (0 for
+ * invalid arguments), and of the device words. */
+size_t arx_ext_region_bytes(int W, size_t max_n);
+size_t arx_ext_words_bytes(void);
+
+/* Fills *x (host struct; no allocation).  dev_words: device buffer (above);
+ * host_region: the HOST address of the page-locked region, whose device
+ * address the library looks up (ARX_EINVAL if it is not page-locked).
+ * nblocks == 0: one 16-byte group of every slot per thread, at most one block
+ * per SM. */
+arx_status arx_ext_init(arx_ext* x, void* dev_words, size_t words_bytes, void* host_region,
+                        size_t region_bytes, int W, size_t max_n, int nblocks);
+
+/* Bound of the GPU's flag waits (ns > 0; default ARX_DEFAULT_TIMEOUT_NS). */
+arx_status arx_ext_set_timeout(arx_ext* x, uint64_t ns);
+
+/* Producer side, host only (never enqueues GPU work; any host thread):
+ *  arx_ext_wait_free  blocks until bank seq & 1 may be written for step seq
+ *                     (consumed >= seq - 2), or returns ARX_ETIMEOUT after
+ *                     wait_ns;
+ *  arx_ext_slot       host address of recv[seq & 1][rank] (NULL for bad
+ *                     arguments), for a producer that writes in place;
+ *  arx_ext_publish    release-stores flag[rank] = seq: everything the calling
+ *                     thread wrote before (the slot) is visible to the GPU
+ *                     once it sees the flag;
+ *  arx_ext_post       arx_ext_wait_free, a copy of n bf16 from src into the
+ *                     slot, arx_ext_publish;
+ *  arx_ext_publish_all  arx_ext_wait_free, then arx_ext_publish for every
+ *                     rank: for a producer that wrote all W slots of the
+ *                     step in place (through arx_ext_slot).
+ * A producer must publish steps of one rank in order, each once. */
+arx_status arx_ext_wait_free(const arx_ext* x, uint32_t seq, uint64_t wait_ns);
+void* arx_ext_slot(const arx_ext* x, uint32_t seq, int rank);
+arx_status arx_ext_publish(const arx_ext* x, int rank, uint32_t seq);
+arx_status arx_ext_post(const arx_ext* x, int rank, uint32_t seq, const void* src, size_t n,
+                        uint64_t wait_ns);
+arx_status arx_ext_publish_all(const arx_ext* x, uint32_t seq, uint64_t wait_ns);
+
+/* Consumer side: enqueues the next step on `stream` (graph-capturable: the
+ * step number is read on the device).  out: device pointer to n bf16, not
+ * overlapping the region or the words; 0 < n <= max_n (n == 0: ARX_OK, no
+ * launch).  Every step of a context must use the same n as its producer
+ * posted.  Steps of one context must be serialised (one stream). */
+arx_status arx_ext_step(arx_ext* x, void* out, size_t n, void* stream);
+
+/* Synchronises `stream` and reads the device words (as arx_ctx_query);
+ * a nonzero error word is kept in x->failed_err. */
+arx_status arx_ext_query(arx_ext* x, uint32_t* seq, uint32_t* dev_err, void* stream);
+
+/* Zeroes the device words (enqueued on `stream`, which it then
+ * synchronises) and the region's flags and `consumed`; clears failed_err.
+ * Call it with no step of the context in flight and no producer running;
+ * steps then start again at 1. */
+arx_status arx_ext_reset(arx_ext* x, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Allocation-free protocol step.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory at the time
  * they call: a serving engine that reserved nearly all of HBM for its own pool
@@ -364,9 +506,12 @@ arx_status arx_watch_step(const arx_ctx* ctx, uint32_t target_seq, uint64_t stal
  *               the step's device error word (0 = success; layout as for
  *               arx_step) when the stream reaches it.  NULL skips it.
  *   stream      cudaStream_t as void*.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  Every call shares the array and
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress, with the calling thread's device current); nothing is
+ * cached, so a context torn down by cudaDeviceReset and created again is
+ * served at the array's new address (its contents do not survive the reset).
+ * The first call in a context may load this library's device code: make it
+ * before any stream capture.  Every call shares the array and
  * first clears its protocol words, so each call is a fresh protocol instance;
  * calls that overlap on the GPU (several streams, or unordered host threads)
  * race on the array and must be serialised by the caller.

@@ -116,14 +116,15 @@ static void step_cases(int W, size_t n) {
   CHECK_CUDA(cudaMemset(ws, 0, ws_bytes));
   arx_ctx ctx;
   CHECK_ARX(arx_ctx_init(&ctx, ws, ws_bytes, W, n, 0));
-  const int modes[3] = {ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED};
-  for (int step = 0; step < 4; ++step) {
+  const int modes[5] = {ARX_SYNC_SEMAPHORE, ARX_SYNC_PAD, ARX_SYNC_PAD_FENCED, ARX_SYNC_CLUSTER,
+                        ARX_SYNC_SEMAPHORE_GLOBAL};
+  for (int step = 0; step < 6; ++step) {
     for (int r = 0; r < W; ++r) {
       for (size_t i = 0; i < n; ++i) host[r][i] = pattern((uint32_t)(1000 + step * 17 + r), (uint32_t)i);
       CHECK_CUDA(cudaMemcpy(dev[r], host[r], n * 2, cudaMemcpyHostToDevice));
     }
     oracle_reduce(hs, W, want, n);
-    if (step < 3) {
+    if (step < 5) {
       CHECK_ARX(arx_ctx_set_sync(&ctx, modes[step]));
       CHECK_ARX(arx_step(&ctx, (const void* const*)dev, out, n, NULL));
       uint32_t seq = 0, err = 0;
@@ -139,7 +140,7 @@ static void step_cases(int W, size_t n) {
     }
     CHECK_CUDA(cudaDeviceSynchronize());
     CHECK_CUDA(cudaMemcpy(got, out, n * 2, cudaMemcpyDeviceToHost));
-    compare(step < 3 ? "arx_step" : "arx_step_noalloc", W, n, got, want);
+    compare(step < 5 ? "arx_step" : "arx_step_noalloc", W, n, got, want);
   }
   CHECK_CUDA(cudaFree(ws));
   CHECK_CUDA(cudaFree(out));
@@ -170,6 +171,52 @@ static void host_case(int W, size_t n) {
   free(want);
 }
 
+/* External-writer form: this thread is the producer (posts steps 1 and 2,
+ * the two banks, before the GPU runs), then the GPU consumes both steps. */
+static void ext_case(int W, size_t n) {
+  const size_t rb = arx_ext_region_bytes(W, n);
+  void* region = NULL;
+  void* words = NULL;
+  void* out = NULL;
+  CHECK_CUDA(cudaHostAlloc(&region, rb, cudaHostAllocDefault));
+  memset(region, 0, rb);
+  CHECK_CUDA(cudaMalloc(&words, arx_ext_words_bytes()));
+  CHECK_CUDA(cudaMemset(words, 0, arx_ext_words_bytes()));
+  CHECK_CUDA(cudaMalloc(&out, 2 * n * 2));
+  arx_ext x;
+  CHECK_ARX(arx_ext_init(&x, words, arx_ext_words_bytes(), region, rb, W, n, 0));
+  uint16_t* part[ARX_MAX_W];
+  uint16_t* want[2];
+  uint16_t* got = (uint16_t*)malloc(n * 2);
+  for (int s = 0; s < 2; ++s) {
+    want[s] = (uint16_t*)malloc(n * 2);
+    for (int r = 0; r < W; ++r) {
+      part[r] = (uint16_t*)malloc(n * 2);
+      for (size_t i = 0; i < n; ++i) part[r][i] = pattern((uint32_t)(9000 + 31 * s + r), (uint32_t)i);
+      CHECK_ARX(arx_ext_post(&x, r, (uint32_t)(s + 1), part[r], n, 1000000000ull));
+    }
+    oracle_reduce((const uint16_t* const*)part, W, want[s], n);
+    for (int r = 0; r < W; ++r) free(part[r]);
+  }
+  CHECK_ARX(arx_ext_step(&x, out, n, NULL));
+  CHECK_ARX(arx_ext_step(&x, (uint16_t*)out + n, n, NULL));
+  uint32_t seq = 0, err = 0;
+  CHECK_ARX(arx_ext_query(&x, &seq, &err, NULL));
+  if (seq != 2 || err != 0) {
+    fprintf(stderr, "arx_ext_step W=%d: seq %u err 0x%08x\n", W, seq, err);
+    ++failures;
+  }
+  for (int s = 0; s < 2; ++s) {
+    CHECK_CUDA(cudaMemcpy(got, (uint16_t*)out + (size_t)s * n, n * 2, cudaMemcpyDeviceToHost));
+    compare("arx_ext_step", W, n, got, want[s]);
+    free(want[s]);
+  }
+  free(got);
+  CHECK_CUDA(cudaFree(out));
+  CHECK_CUDA(cudaFree(words));
+  CHECK_CUDA(cudaFreeHost(region));
+}
+
 int main(void) {
   const size_t sizes[4] = {1, 13, 4099, 131072 + 5};
   for (int W = 1; W <= ARX_MAX_W; ++W)
@@ -180,6 +227,8 @@ int main(void) {
   step_cases(8, 131072);
   step_cases(3, 5003);
   host_case(8, 131072);
+  ext_case(8, 131072);
+  ext_case(3, 4099);
   /* Argument errors come back as status codes. */
   if (arx_reduce(NULL, 2, (void*)16, 8, NULL) != ARX_EINVAL) {
     fprintf(stderr, "null slot array not rejected\n");

@@ -28,7 +28,8 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for must in ("arx_reduce", "arx_step", "arx_ctx_init", "arx_ctx_query",
-                 "arx_ctx_workspace_bytes", "arx_status_string"):
+                 "arx_ctx_workspace_bytes", "arx_status_string", "arx_ext_step", "arx_ext_post",
+                 "arx_step_noalloc"):
         assert must in names
 
 
@@ -254,3 +255,35 @@ def test_plan_checks_its_arguments_once(arx):
     x = torch.zeros(2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         arx.arx_reduce_plan([x[0], x[1]], x[0])
+
+
+def test_external_writer_layout_and_rejections(arx):
+    # Sizes: 1 KiB of control words, then two banks of W slots of max_n
+    # elements rounded up to 128 (the header's layout).
+    W, n = 8, 131072
+    assert arx.arx_ext_region_bytes(W, n) == 1024 + 2 * W * n * 2
+    assert arx.arx_ext_region_bytes(3, 100) == 1024 + 2 * 3 * 128 * 2
+    assert arx.arx_ext_region_bytes(0, n) == 0 and arx.arx_ext_region_bytes(9, n) == 0
+    assert arx.arx_ext_words_bytes() == 256
+    x = arx.arx_ext()
+    init = arx.lib.arx_ext_init
+    region = (ctypes.c_uint8 * (arx.arx_ext_region_bytes(2, 64) + 256))()
+    R = (ctypes.addressof(region) + 255) // 256 * 256
+    rb = arx.arx_ext_region_bytes(2, 64)
+    assert init(ctypes.byref(x), FAKE, 256, R, rb, 0, 64, 1) == arx.ARX_EINVAL           # W
+    assert init(ctypes.byref(x), FAKE + 16, 256, R, rb, 2, 64, 1) == arx.ARX_EINVAL      # alignment
+    assert init(ctypes.byref(x), FAKE, 255, R, rb, 2, 64, 1) == arx.ARX_EINVAL           # words too small
+    assert init(ctypes.byref(x), FAKE, 256, R, rb - 1, 2, 64, 1) == arx.ARX_EINVAL       # region too small
+    assert init(ctypes.byref(x), FAKE, 256, 0, rb, 2, 64, 1) == arx.ARX_EINVAL           # no region
+    # Ordinary (pageable) host memory is not a region the GPU can read.
+    assert init(ctypes.byref(x), FAKE, 256, R, rb, 2, 64, 1) == arx.ARX_EINVAL
+    assert "page-locked" in arx.arx_last_error()
+    # An uninitialised context is refused by every call.
+    y = arx.arx_ext()
+    assert arx.lib.arx_ext_step(ctypes.byref(y), FAKE, 64, None) == arx.ARX_ESTATE
+    assert arx.lib.arx_ext_post(ctypes.byref(y), 0, 1, R, 64, 10**6) == arx.ARX_ESTATE
+    assert arx.lib.arx_ext_publish(ctypes.byref(y), 0, 1) == arx.ARX_ESTATE
+    assert arx.lib.arx_ext_publish_all(ctypes.byref(y), 1, 10**6) == arx.ARX_ESTATE
+    assert arx.lib.arx_ext_wait_free(ctypes.byref(y), 1, 10**6) == arx.ARX_ESTATE
+    assert arx.lib.arx_ext_slot(ctypes.byref(y), 1, 0) is None
+    assert arx.lib.arx_ext_set_timeout(ctypes.byref(y), 5) == arx.ARX_ESTATE

@@ -114,7 +114,7 @@ def test_random_steps_stay_in_bounds(checked, arx):
         W = int(rng.integers(1, 9))
         n = int(rng.integers(1, 40000)) if case % 6 else 1 << 20
         B = int(rng.integers(0, 8))
-        mode = int(rng.integers(0, 4))   # every barrier variant, the cluster one included
+        mode = int(rng.integers(0, 5))   # every barrier variant, the cluster ones included
         in_off, out_off = int(rng.integers(0, 8)), int(rng.integers(0, 8))
         ws = torch.zeros(checked.arx_ctx_workspace_bytes(W, n, B), dtype=torch.uint8, device=dev)
         ctx = arx.arx_ctx()

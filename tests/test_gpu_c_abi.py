@@ -1,9 +1,10 @@
 """The C ABI driven from a plain C program (tests/c_abi/abi_smoke.c): no Python
 binding and no torch on the path.  The program allocates with the CUDA runtime,
 calls arx_reduce (separate and in-place output, every W, ragged n),
-arx_step in each barrier variant, arx_step_noalloc and arx_reduce_host on
-page-locked buffers, and compares every output bit for bit with the CPU oracle's
-C library.  Compiled with gcc on the machine that runs it."""
+arx_step in each barrier variant, arx_step_noalloc, arx_reduce_host on
+page-locked buffers and the external-writer form (arx_ext_post as the producer,
+arx_ext_step as the consumer), and compares every output bit for bit with the
+CPU oracle's C library.  Compiled with gcc on the machine that runs it."""
 
 import os
 import shutil

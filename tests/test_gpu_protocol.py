@@ -13,10 +13,12 @@
 * Failure detection without any GPU fault: a missing end-barrier signal
   makes the bounded waits expire (ARX_ETIMEOUT read by the host, context
   usable after a reset); a corrupted epoch reports ARX_ESTATE.
-* All of the above in each barrier variant (``ARX_SYNC_SEMAPHORE``,
-  ``ARX_SYNC_PAD``, ``ARX_SYNC_PAD_FENCED``: common.cuh's Semaphore barriers,
-  or triton_barrier.py's pad barrier in its Patterns 0/1/2, relaxed or
-  acq_rel), and switching variants between steps of one context.
+* All of the above in each barrier variant (``ARX_SYNC_SEMAPHORE`` with the
+  flags in the cluster's shared memory, ``ARX_SYNC_SEMAPHORE_GLOBAL`` with
+  them in global memory: common.cuh's Semaphore barriers;
+  ``ARX_SYNC_PAD``, ``ARX_SYNC_PAD_FENCED``: triton_barrier.py's pad barrier
+  in its Patterns 0/1/2, relaxed or acq_rel; ``ARX_SYNC_CLUSTER``), and
+  switching variants between steps of one context.
 * The slot banks in a separate buffer (``arx_ctx_init_split``), in device
   memory or in page-locked host memory (arx.cu's GB10 layout: pinned host
   slots the GPU writes and reads over the CPU-GPU link): single steps, the
@@ -37,8 +39,9 @@ from test_gpu_reduce import assert_bits_equal
 pytestmark = pytest.mark.gpu
 
 M32 = 0xFFFFFFFF
-SYNCS = ["semaphore", "pad", "pad_fenced", "cluster"]
-FLAG_SYNCS = SYNCS[:3]          # the variants with in-protocol fault injection
+SYNCS = ["semaphore", "pad", "pad_fenced", "cluster", "semaphore_global"]
+FLAG_SYNCS = ["semaphore", "pad", "pad_fenced", "semaphore_global"]   # with in-protocol fault injection
+SEM_SYNCS = ("semaphore", "semaphore_global")     # the variants that advance the Semaphore words
 
 
 @pytest.fixture(scope="module")
@@ -207,12 +210,12 @@ def test_random_small_steps(arx, dev):
 
 
 def test_contexts_step_concurrently_on_separate_streams(arx, dev):
-    # Independent contexts share no state: three of them (different W and
-    # barrier variants) run 200 steps each on three streams at once -- two
-    # cooperative grids and one of clusters resident together, each waiting
-    # only on its own blocks -- and every output of all three is checked.
+    # Independent contexts share no state: four of them (different W and
+    # barrier variants) run 200 steps each on four streams at once -- two
+    # cooperative grids and two of clusters resident together, each waiting
+    # only on its own blocks -- and every output of all four is checked.
     steps = 200
-    cfg = [(8, 65536, "semaphore"), (3, 40000, "pad"), (5, 30000, "cluster")]
+    cfg = [(8, 65536, "semaphore"), (3, 40000, "pad"), (5, 30000, "cluster"), (6, 20000, "semaphore_global")]
     ctxs, ins, outs, wants = [], [], [], []
     for W, n, sync in cfg:
         c = Ctx(arx, dev, W, n, 0, sync)
@@ -324,7 +327,7 @@ def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync, slots):
         assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s}")
         _compare_to_model(c.words(), st)
-    assert (c.words()["flag"] == (2 * W * k if sync == "semaphore" else 0)).all()
+    assert (c.words()["flag"] == (2 * W * k if sync in SEM_SYNCS else 0)).all()
     # Staggered staging counts: zero between steps (the last block out of a
     # staggered step clears its bank), host slots or not.
     assert not c.words()["stagger"].any()
@@ -373,11 +376,11 @@ def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
     st, seq, err = arx.arx_ctx_query(c.ctx)
     assert st == arx.ARX_ETIMEOUT
     # stage: the end-barrier wait (2 on the Semaphores, 9 on the pad)
-    assert err & 0xFF == arx.ARX_ETIMEOUT and (err >> 8) & 15 == (2 if sync == "semaphore" else 9)
+    assert err & 0xFF == arx.ARX_ETIMEOUT and (err >> 8) & 15 == (2 if sync in SEM_SYNCS else 9)
     assert seq == 2                                  # the kernel still finished
     w = c.words()
     assert w["blocks"] == [0, 0]
-    if sync == "semaphore":
+    if sync in SEM_SYNCS:
         assert not w["pad"].any()
     # The context remembers the failure: the next step is refused on the host,
     # with nothing launched (output and protocol words untouched).
@@ -457,8 +460,8 @@ def test_switching_sync_modes_between_steps(arx, dev):
     W, n = 6, 30011
     c = Ctx(arx, dev, W, n, 3)
     st = model.State(W=W, B=c.B)
-    for s, sync in enumerate(["semaphore", "pad", "cluster", "pad_fenced", "semaphore", "cluster", "pad_fenced",
-                              "pad", "cluster", "semaphore"]):
+    for s, sync in enumerate(["semaphore", "pad", "cluster", "pad_fenced", "semaphore_global", "semaphore",
+                              "cluster", "pad_fenced", "semaphore_global", "pad", "cluster", "semaphore"]):
         c.set_sync(sync)
         x = sp.partials(W, n, "normal", seed=300 + s)
         out = _step(arx, c, x, dev)
@@ -483,24 +486,24 @@ def test_mixed_variants_in_one_graph(arx, dev):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for t in range(steps):
-            c.set_sync(SYNCS[t % 4])
+            c.set_sync(SYNCS[t % len(SYNCS)])
             arx.arx_step(c.ctx, [xd[t % 3][r] for r in range(W)], outs[t], stream=s)
     g.replay()
     torch.cuda.synchronize()
     assert arx.arx_ctx_query(c.ctx)[:3] == (arx.ARX_OK, steps, 0)
     got = outs.cpu().view(torch.int16).numpy().view(np.uint16)
     for t in range(steps):
-        assert_bits_equal(got[t], wants[t % 3], f"step {t} ({SYNCS[t % 4]})")
+        assert_bits_equal(got[t], wants[t % 3], f"step {t} ({SYNCS[t % len(SYNCS)]})")
     st = model.State(W=W, B=c.B)
     for t in range(steps):
-        model.step(st, list(sp.to_u16_numpy(xs[t % 3])), sync=SYNCS[t % 4])
+        model.step(st, list(sp.to_u16_numpy(xs[t % 3])), sync=SYNCS[t % len(SYNCS)])
     _compare_to_model(c.words(), st)
 
 
 def test_unknown_sync_mode_is_rejected(arx, dev):
     c = Ctx(arx, dev, 2, 64, 1)
     with pytest.raises(arx.ArxError):
-        arx.arx_ctx_set_sync(c.ctx, 4)
+        arx.arx_ctx_set_sync(c.ctx, len(SYNCS))
     assert c.ctx.sync_mode == arx.ARX_SYNC_SEMAPHORE
 
 
@@ -578,7 +581,7 @@ def test_ten_thousand_steps_in_one_graph(arx, dev, graph_workload, sync, slots):
     assert bad.size == 0, f"{bad.size} of {steps} steps differ; first step {int(bad[0])}"
     w = c.words()
     assert not w["pad"].any(), "signal pad must be all zero after the last step"
-    flags = 2 * W8 * steps if sync == "semaphore" else 0   # the pad variants leave the Semaphores alone
+    flags = 2 * W8 * steps if sync in SEM_SYNCS else 0   # the pad variants leave the Semaphores alone
     assert (w["flag"] == flags).all() and (w["counter"] == w["flag"]).all()
     assert (w["epoch"] == steps % 2).all() and w["blocks"] == [0, 0]
     assert w["published"] == steps
