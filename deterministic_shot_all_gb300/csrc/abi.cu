@@ -301,17 +301,24 @@ int auto_blocks(int W, size_t max_n, arx_status* s) {
 }
 
 // Block groups of the staggered staging for slots in host memory: about
-// 128 KiB of staged data per group (the link writes that in about the time
-// one group's hand-off to the next takes), at most 16 and at most B; 0 (all
-// at once) below two.  Measured on GB300 over NVLink-C2C (W = 8
-// [32, 4096]: 25.6 us per step at once, 20.3-20.9 at 16 groups; W = 4:
-// 14.5 -> 11.8-12.2 us at 8 groups; W = 8 at 2^19: 85 -> 61 us at 16).
+// 128 KiB of staged data per group, at most B; 0 (all at once) below two.
+// Group g starts writing at T0 + g * stagger_ns, stagger_ns the time the
+// GPU-to-host direction of NVLink-C2C takes to write one group's bytes at
+// kHostWriteBytesPerNs.  Measured on GB300 (W = 8 [32, 4096], 16 groups of
+// 128 KiB): 160 bytes/ns 18.5-18.8 us per step, 190 18.7-19.4, 220 and 250
+// slower (groups crowd the link), 120 slower (the link idles between
+// groups).  The link's one-way copy rate is 190-206 GB/s.
+constexpr uint64_t kHostWriteBytesPerNs = 160;
+
 int stagger_groups(int W, size_t n, int B) {
   const size_t bytes = size_t(W) * n * 2;
   size_t K = (bytes + (size_t(64) << 10)) >> 17;  // nearest multiple of 128 KiB
-  if (K > 16) K = 16;
   if (K > size_t(B)) K = size_t(B);
   return K < 2 ? 0 : int(K);
+}
+
+uint64_t stagger_ns(int W, size_t n, int K) {
+  return K < 2 ? 0 : uint64_t(size_t(W) * n * 2 / size_t(K)) / kHostWriteBytesPerNs;
 }
 
 arx_status check_ctx(const arx_ctx* ctx) {
@@ -500,6 +507,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.stagger = ctx->slots_where == ARX_SLOTS_HOST && ctx->sync_mode != ARX_SYNC_CLUSTER
                   ? stagger_groups(ctx->W, n, ctx->nblocks)
                   : 0;
+  c.stagger_ns = stagger_ns(ctx->W, n, c.stagger);
   ARX_SET_BOUNDS_COUNTER(c);
   e = arx::launch_step(c, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "arx_step launch");

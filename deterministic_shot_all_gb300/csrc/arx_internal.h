@@ -46,6 +46,7 @@ struct StepCall {
   int fault_rank;
   int sync_mode;  // ARX_SYNC_*
   int stagger;    // K >= 2: K block groups start staging in turn (slots in host memory); else 0
+  uint64_t stagger_ns;  // time between two groups' starts
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif

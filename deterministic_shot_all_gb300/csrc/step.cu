@@ -25,17 +25,20 @@
 //     completed (arx.cu "last block out").
 //
 // Barrier variants (the context's sync mode), all with the same data path:
-//  * Semaphore (default): steps 2 and 4 as above, with each block's flag held
-//    for the step in its shared memory.  The W blocks of chunk b are one
-//    thread-block cluster; they add to each other's flags through
-//    distributed shared memory and the owner polls its own.  The flag and
-//    counter are loaded at entry and written back at exit, so the words in
-//    memory follow the same arithmetic.  The cluster barrier runs in two
-//    split phases: arrive after zeroing the shared flag, wait before the
-//    first remote add (every flag is in place); arrive after the last remote
-//    add, wait just before exit (no add reaches an exited block).  Step 6 is
-//    that last wait: it also tells every block of the chunk that all reads of
-//    the chunk's slots are done, which is the pad barrier's Pattern 2.
+//  * Semaphore (default): steps 2 and 4 with each block's flag held for the
+//    step in its shared memory.  The W blocks of chunk b are one
+//    thread-block cluster.  Start stage: the W arrivals at the cluster's
+//    hardware barrier are its W signals (every block's zeroed flag is in
+//    place once it completes).  End stage: every block adds 1 to each peer's
+//    flag through distributed shared memory, then the cluster barrier
+//    (release arrival, acquire wait) orders the staged slots and the adds;
+//    the owner then checks flag - counter >= 2W, bounded, which waits only
+//    if a signal is missing.  The flag and counter are loaded at entry and
+//    written back at exit, so the words in memory follow the same
+//    arithmetic.  No add is in flight after the end barrier, so no exit
+//    barrier is needed; the kernel boundary stands in for Pattern 2 (the
+//    next kernel on the stream starts only after every block of this one
+//    has finished reading the slots).
 //  * Semaphore, global: steps 2 and 4 with the flags in the workspace (as the
 //    page keeps them for peers on other GPUs), step 6 a relaxed pad barrier.
 //    Also used for host-slot steps that stage in turn (their waits cross
@@ -106,8 +109,6 @@ enum SyncMode : int {
 // 16-byte vectors each thread loads before storing them while staging.
 constexpr int kStageBatch = 4;
 
-// Most block groups of the staggered staging (host slots).
-constexpr int kMaxStagger = 16;
 
 // Bytes of its input chunk a block prefetches into L2 before the dependency
 // wait: its first two staging batches.  Only for messages whose W inputs
@@ -124,12 +125,13 @@ struct Header {  // first bytes of the workspace (256 reserved)
   uint32_t blocks[2];  // blocks past staging / blocks finished
   uint32_t published;  // last staged seq
   uint32_t unused[27];
-  // Byte 128: staging-done counts of the block groups of a staggered step,
-  // in bank seq & 1; the step's last block out zeroes the bank, so both are
-  // zero between steps.
-  uint32_t stagger[2][kMaxStagger];
+  // Byte 128: the global timer value at which a staggered step's first block
+  // arrived (the groups' start times count from it); the step's last block
+  // out zeroes it, so it is zero between steps.
+  unsigned long long stagger_t0;
+  uint32_t unused2[30];
 };
-static_assert(offsetof(Header, stagger) == 128 && sizeof(Header) <= 256, "header layout");
+static_assert(offsetof(Header, stagger_t0) == 128 && sizeof(Header) == 256, "header layout");
 
 // common.cuh `Semaphore`: 128-byte aligned flag + counter; the counter is
 // read and written only by the owning block.
@@ -152,6 +154,7 @@ struct StepArgs {
   int out_vec;           // out is 16-byte aligned
   int prefetch;          // L2 prefetch of the input chunks (small messages)
   uint32_t stagger;      // K >= 2 block groups stage in turn (staggering kernels only)
+  uint64_t stagger_ns;   // time between two groups' starts
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   constexpr bool kDsm = kSync == kSyncSemaphore;    // clusters too; Semaphores in shared memory
   constexpr bool kSemGlobal = kSync == kSyncSemaphoreGlobal;
   constexpr bool kFencedAll = kSync == kSyncPadFenced;
-  static_assert(!(kStagger && (kCluster || kDsm)), "staggered staging waits across clusters");
+  static_assert(!(kStagger && (kCluster || kDsm)), "the cluster-launched variants stage all at once");
   const uint32_t b = blockIdx.x, r = blockIdx.y;
   const uint32_t B = uint32_t(a.B);
   const uint32_t tid = threadIdx.x, warp = tid / 32u, lane = tid % 32u;
@@ -329,21 +332,11 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   uint32_t base = 0;
   uint32_t flag_in = 0;  // Semaphore variant: the flag as the previous step left it
   if constexpr (kDsm) {
-    // The shared word counts this step's adds from zero; the owner keeps the
-    // flag and counter of the previous step in registers, so the words obey
-    // the page's arithmetic -- flag - counter = (flag_in + adds) - counter,
-    // i.e. adds - base with base = counter - flag_in.  Zero the word and
-    // arrive at the cluster barrier at once (release: the zero is visible to
-    // the cluster before any peer's add can reach it); the global words are
-    // loaded after the arrival, so their latency overlaps the barrier.  The
-    // wait comes after the first staging loads below.
+    // The shared word counts this step's end-stage adds from zero; the owner
+    // keeps the flag and counter of the previous step in registers, so the
+    // words obey the page's arithmetic: flag - counter = (flag_in + W + adds)
+    // - counter, i.e. W + adds - base with base = counter - flag_in.
     if (tid == owner) st_shared(flag_sh, 0u);
-    __syncwarp();  // the cluster barrier instructions are warp-aligned
-    cluster_arrive_release();
-    if (tid == owner) {
-      flag_in = own.flag;
-      base = own.counter - flag_in;
-    }
   }
 
   // The first batch of this block's staging loads.  They read only the
@@ -361,17 +354,22 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 
   // 2. start barrier.
   if constexpr (kDsm) {
-    // PullController start stage, unfenced, on the shared-memory flags: once
-    // every block of the cluster has its flag in place (the hardware
-    // barrier), lane 0 of warp q < W adds 1 to block q's flag; lane 0 of
-    // warp r waits for W.
+    // PullController start stage (unfenced): its W signals are the W blocks'
+    // arrivals at the cluster barrier, which every block has passed once
+    // this wait returns -- counted into the flag as W at write-back.  The
+    // owner's warp arrives with release, so the zeroed word is in place
+    // before any peer's add can reach it; the other warps arrive relaxed (a
+    // release arrival by every warp measured 2-4 % slower).  The global words
+    // are loaded between arrival and wait and first used at the end stage,
+    // so their latency hides behind the barrier and the staging.
+    __syncwarp();  // the cluster barrier instructions are warp-aligned
+    if (warp == r) cluster_arrive_release(); else cluster_arrive_relaxed();
+    if (tid == owner) {
+      flag_in = own.flag;
+      base = own.counter - flag_in;
+    }
     __syncwarp();
     cluster_wait();
-    if (lane == 0 && warp < uint32_t(W)) {
-      red_add_relaxed_cluster(cluster_peer_address(flag_sh, warp), 1u);
-      if (warp == r && !shared_semaphore_wait<false>(flag_sh, base, uint32_t(W), a.timeout_ns))
-        record_error(&hdr->err, kErrTimeout, kStartWait, r, b);
-    }
   } else if constexpr (kCluster) {
     // The W blocks of chunk b are one cluster: its hardware barrier, relaxed.
     cluster_arrive_relaxed();
@@ -399,26 +397,36 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   uint16_t* bank = slots + size_t(par) * size_t(W) * stride;
 
   // Staggered staging (slots in host memory): the blocks form K groups by
-  // chunk; group g starts writing its slots once every block of group g - 1
-  // has issued its own (counted in hdr->stagger[par][g - 1]), so one group's
-  // writes to host memory overlap the previous group's reads over the
-  // full-duplex link.  A scheduling wait only -- the barriers order the
-  // data -- and bounded like every other wait.  Compiled only into the
-  // kernels of host-slot steps: the Semaphore variant ran 4-10 % slower
-  // with the unused code present.
+  // chunk, and group g starts writing its slots at T0 + g * stagger_ns,
+  // where T0 is the global timer when the step's first block got here
+  // (compare-and-swapped into the header) and stagger_ns is the time the
+  // link takes to write one group's staged bytes.  So the writes to host
+  // memory go out at about the link's rate, group after group, and each
+  // group's reads (after its end barrier) overlap the later groups' writes
+  // on the full-duplex link.  A scheduling delay only -- the barriers order
+  // the data -- bounded by the context's timeout (error stage 10 if a stale
+  // T0 asks for longer), and no block waits for another.  Measured (W = 8
+  // [32, 4096], GB300): 18.5-18.8 us per step against 22.2 us when each
+  // group waited for the previous one's count through L2 (about 1.1 us per
+  // hand-off, 16 hand-offs) and 23.5 us with every group at once.  Compiled
+  // only into the kernels of host-slot steps.
   uint32_t K = 0, grp = 0;
   if constexpr (kStagger) {
     K = a.stagger;
     grp = b * K / B;
-    if (grp > 0u) {
-      if (tid == 0) {
-        const uint32_t g0 = grp - 1u;  // blocks b with b * K / B == g0, W of each
-        const uint32_t nb = ((g0 + 1u) * B + K - 1u) / K - (g0 * B + K - 1u) / K;
-        if (!count_wait(&hdr->stagger[par][g0], uint32_t(W) * nb, a.timeout_ns))
+    if (tid == 0) {
+      const unsigned long long now = global_timer_ns();
+      const unsigned long long old = atomicCAS(&hdr->stagger_t0, 0ull, now);
+      const unsigned long long target = (old ? old : now) + grp * a.stagger_ns;
+      for (uint64_t spins = 0; global_timer_ns() < target; ++spins) {
+        if (global_timer_ns() - now > a.timeout_ns || spins > spin_cap(a.timeout_ns)) {
           record_error(&hdr->err, kErrTimeout, kStaggerWait, r, b);
+          break;
+        }
+        __nanosleep(32);
       }
-      __syncthreads();
     }
+    __syncthreads();
   }
 
   // 3. stage rank r's chunk b into slots[par][r].
@@ -458,11 +466,6 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   }
   // 4. end barrier, fenced: every thread's staging precedes the release.
   __syncthreads();
-  // This block's staging is issued: count it for the next group (a thread
-  // no barrier uses).
-  if constexpr (kStagger) {
-    if (grp + 1u < K && tid == uint32_t(kThreads) - 1u) red_add_relaxed_gpu(&hdr->stagger[par][grp], 1u);
-  }
   if constexpr (kCluster) {
     // Release on arrive (after the block barrier: the whole block's staging),
     // acquire on wait; the published count runs between the two.
@@ -488,27 +491,39 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       }
     }
   } else if constexpr (kDsm) {
-    // PullController end stage on the shared-memory flags: release adds at
-    // cluster scope (after the block barrier: the whole block's staging),
-    // then the cluster barrier's second arrival -- every write this block
-    // makes to a peer's shared memory is issued before it, so once all have
-    // arrived no block still writes into another (the wait is at exit).
-    // Lane 0 of warp r waits for 2W with acquire and advances the counter.
+    // PullController end stage: lane 0 of warp q < W adds 1 to block q's
+    // flag through distributed shared memory, then every thread arrives at
+    // the cluster barrier with release (after the block barrier: the whole
+    // block's staging, and this block's adds, are ordered before the
+    // arrival) and waits with acquire.  When the wait returns, every add of
+    // the cluster has landed and every staged slot of the chunk is visible;
+    // no block writes into another block's shared memory after it, so no
+    // exit barrier is needed.  The owner then checks flag - counter >= 2W --
+    // it passes at once unless a signal is missing (the fault knob), in
+    // which case it waits, bounded, and reports ARX_ETIMEOUT -- and advances
+    // the counter.  Measured (W = 8 [32, 4096], GB300, A/B of library builds
+    // in one process): 4.1 us per step with this form; 4.4-4.5 us with the
+    // owner polling its flag for release adds and no hardware barrier after
+    // staging, 4.6 us with the adds issued after the arrival (the check then
+    // waits for them, and an exit barrier must keep them from landing in an
+    // exited block), 5.6 us with the flags in global memory; the cluster
+    // variant, with no flag traffic at all, 3.5 us.
     if (lane == 0 && warp < uint32_t(W) && int(r) != a.fault_rank)
-      red_add_release_cluster(cluster_peer_address(flag_sh, warp), 1u);
+      red_add_relaxed_cluster(cluster_peer_address(flag_sh, warp), 1u);
     __syncwarp();
     cluster_arrive_release();
+    if (tid == 32u && atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
+      // Last block past the copy publishes seq (only the host watchdog reads it).
+      hdr->blocks[0] = 0u;
+      st_relaxed_gpu(&hdr->published, seq);
+    }
+    __syncwarp();
+    cluster_wait();
     if (tid == owner) {
-      if (shared_semaphore_wait<true>(flag_sh, base, 2u * uint32_t(W), a.timeout_ns)) {
+      if (shared_semaphore_wait<false>(flag_sh, base, uint32_t(W), a.timeout_ns)) {
         base += 2u * uint32_t(W);  // the counter after this step
       } else {
         record_error(&hdr->err, kErrTimeout, kEndWait, r, b);
-      }
-    } else if (tid == 1) {
-      // Last block past the copy publishes seq (only the host watchdog reads it).
-      if (atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
-        hdr->blocks[0] = 0u;
-        st_relaxed_gpu(&hdr->published, seq);
       }
     }
   } else if (lane == 0 && warp < uint32_t(W)) {
@@ -592,34 +607,32 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
                             kPadWait);
   } else if (tid == 32u) {
     epoch[r * B + b] = (s_epoch + 1u) % 2u;  // PushController::exit
-    // Staggered steps: the fence orders this block's staging count (issued
-    // before the block barriers above) before its exit count, so the last
-    // block out, fenced again, can zero the bank with no count still to land.
+    // Staggered steps: the fence orders this block's read of T0 (before the
+    // block barriers above) before its exit count, so the last block out,
+    // fenced again, zeroes T0 after every block has read it.
     if constexpr (kStagger) __threadfence();
     if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
       hdr->blocks[1] = 0u;
       if constexpr (kStagger) {
         __threadfence();
-#pragma unroll
-        for (int g = 0; g < kMaxStagger; ++g) st_relaxed_gpu(&hdr->stagger[par][g], 0u);
+        hdr->stagger_t0 = 0ull;
       }
       st_relaxed_gpu(&hdr->seq, seq);
     }
   }
-  if constexpr (kCluster || kDsm) {
-    // Every block of the cluster passes this wait before it exits: in the
-    // Semaphore variant no peer can then still be adding to this block's
-    // shared memory.  All arrivals are unconditional (no thread returns
-    // early, and the fault knob only skips an add), so the wait always ends.
+  if constexpr (kCluster) {
+    // All arrivals are unconditional (no thread returns early), so the wait
+    // always ends.
     __syncwarp();
     cluster_wait();
   }
   if constexpr (kDsm) {
     // Write the step's Semaphore words back (common.cuh keeps them in memory
-    // between calls): the flag with every add of the step counted, the
-    // counter advanced by 2W after a successful end stage.
+    // between calls): the flag with every signal of the step counted (W at
+    // the start barrier, the landed end-stage adds), the counter advanced by
+    // 2W after a successful end stage.
     if (tid == owner) {
-      own.flag = flag_in + ld_relaxed_cluster_shared(flag_sh);
+      own.flag = flag_in + uint32_t(W) + ld_relaxed_cluster_shared(flag_sh);
       own.counter = base + flag_in;
     }
   }
@@ -676,9 +689,10 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   a.fault_rank = c.fault_rank;
   for (int r = 0; r < W; ++r)
     if ((reinterpret_cast<uintptr_t>(c.in[r]) & 15u) == 0) a.in_vec_mask |= 1u << r;
-  a.stagger = c.stagger > kMaxStagger ? uint32_t(kMaxStagger) : uint32_t(c.stagger < 0 ? 0 : c.stagger);
+  a.stagger = uint32_t(c.stagger < 0 ? 0 : c.stagger);
   if (a.stagger > uint32_t(c.B)) a.stagger = uint32_t(c.B);
   if (a.stagger < 2u) a.stagger = 0;
+  a.stagger_ns = c.stagger_ns;
   a.prefetch = size_t(W) * c.n * 2u <= kPrefetchMaxBytes;
   a.out_vec = (reinterpret_cast<uintptr_t>(c.out) & 15u) == 0;
 
@@ -710,8 +724,9 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   switch (c.sync_mode) {
     case kSyncSemaphore:
       if (st) {
-        // Staggered staging (slots in host memory) waits across clusters, so
-        // the Semaphores stay in global memory and the grid is cooperative.
+        // Staggered steps (slots in host memory) run the Semaphores in global
+        // memory: 18.5-18.8 us per step against 19.0 with the flags in
+        // shared memory (W = 8 [32, 4096], GB300).
         err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphoreGlobal, true>, a);
       } else {
         cfg.attrs = cattr;

@@ -140,6 +140,9 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  *   5. reduce sub-range r of chunk b over slots[par][0..W-1] into out;
  *   6. pad barrier (0->1 sends, 1->0 waits), epoch[r][b] ^= 1, last block out
  *      stores seq as completed.
+ * This outline is the page's, and the ARX_SYNC_SEMAPHORE_GLOBAL variant's;
+ * the other barrier variants below realise steps 2, 4 and 6 differently
+ * (the default on a thread-block cluster), with the same data path.
  * The output equals arx_reduce's bit for bit.  Every flag wait is bounded by
  * the context's timeout; on expiry the block records ARX_ETIMEOUT in the
  * device error word and carries on, so the kernel always finishes (the
@@ -152,9 +155,9 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  * nblocks) bytes and 256-byte aligned.  Layout (offsets in arx_ctx):
  *   [0, 256)        header, uint32: seq (completed steps), err (device error
  *                   word, 0 = none), blocks[2] (publish / exit counters),
- *                   published (last staged seq); at byte 128
- *                   stagger[2][16] (staging-done counts of a staggered
- *                   host-slot step, zero between steps)
+ *                   published (last staged seq); at byte 128 a uint64,
+ *                   the start time of a staggered host-slot step (zero
+ *                   between steps)
  *   off_epoch       uint32 epoch[W][B]                    (PushController)
  *   off_sem         struct { uint32 flag, counter; } sem[W][B], 128-byte
  *                   stride                                (Semaphore)
@@ -219,11 +222,13 @@ arx_status arx_ctx_init(arx_ctx* ctx, void* ws, size_t ws_bytes, int W, size_t m
  * Everything else as arx_ctx_init; arx_ctx_reset zeroes the words only.
  * Buffers are the caller's and must outlive the context's last step.
  * With the slots in host memory a step of at least 192 KiB of partials
- * stages in turn: its blocks form up to 16 groups by chunk (about 128 KiB of
- * staged data each), and each group starts writing its slots once every
- * block of the previous group has issued its own, so writes to host memory
- * overlap the previous group's reads on the full-duplex link.  Only the
- * start times move; barriers and result are the same. */
+ * stages in turn: its blocks form groups by chunk (about 128 KiB of staged
+ * data each, at most one per block), and group g starts writing its slots at
+ * T0 + g * (the time the GPU-to-host link takes to write one group), T0 the
+ * global timer when the step's first block arrived -- so writes to host
+ * memory go out at about the link's rate and overlap the earlier groups'
+ * reads on the full-duplex link.  Only the start times move; barriers and
+ * result are the same, and no block waits for another to start. */
 #define ARX_SLOTS_DEVICE 0
 #define ARX_SLOTS_HOST 1
 size_t arx_ctx_words_bytes(int W, int nblocks);
@@ -239,30 +244,30 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
  * which of the pages' barriers run, where their words live and in their
  * memory ordering):
  *  ARX_SYNC_SEMAPHORE   (default) common.cuh's PullController over the
- *                       Semaphores for the start (unfenced) and end (release
- *                       adds, acquire waits) barriers, with each Semaphore
- *                       flag held for the step in its block's shared memory:
- *                       the W blocks of a chunk are one thread-block cluster
- *                       and add to each other's flags through distributed
- *                       shared memory.  The flag and counter are loaded from
+ *                       Semaphores, with each Semaphore flag held for the
+ *                       step in its block's shared memory: the W blocks of a
+ *                       chunk are one thread-block cluster.  Start stage
+ *                       (unfenced): the W blocks' arrivals at the cluster's
+ *                       hardware barrier are its W signals.  End stage: each
+ *                       block adds 1 to every peer's flag through distributed
+ *                       shared memory, the cluster barrier (release arrival,
+ *                       acquire wait) makes the staged slots and the adds
+ *                       visible, and the owner checks flag - counter >= 2W,
+ *                       a bounded wait that waits only when a signal is
+ *                       missing (the fault knob skips one, as in the flag
+ *                       modes below).  The flag and counter are loaded from
  *                       the workspace at entry and written back at exit, so
- *                       the words follow the same arithmetic as in the
- *                       global form.  The cluster's hardware barrier runs
- *                       twice, split into arrive and wait (between them the
- *                       block stages, or reduces): once so that every flag is
- *                       loaded before a peer adds to it, and once before exit
- *                       so that no peer still adds to an exited block.  Both
- *                       complete whatever the flags do (every thread arrives
- *                       unconditionally), and every flag wait is bounded, so
- *                       the fault knob works as in the flag modes below.
- *                       Steps with slots in host memory that stage in turn
- *                       (see arx_ctx_init_split) wait across chunks and run
- *                       in the global form (ARX_SYNC_SEMAPHORE_GLOBAL).
+ *                       the words follow the same arithmetic as in the global
+ *                       form.  The hardware barrier's waits complete because
+ *                       every thread arrives unconditionally.  Steps with
+ *                       slots in host memory that stage in turn (see
+ *                       arx_ctx_init_split) run in the global form
+ *                       (ARX_SYNC_SEMAPHORE_GLOBAL), measured faster there.
  *  ARX_SYNC_SEMAPHORE_GLOBAL  the same barriers with the Semaphores in the
  *                       workspace (global memory), as the page keeps them for
- *                       peers on other GPUs; triton_barrier.py's
- *                       blockwise_barrier, Pattern 2, relaxed, at exit; a
- *                       cooperative grid.
+ *                       peers on other GPUs: release adds and acquire polls
+ *                       through L2; triton_barrier.py's blockwise_barrier,
+ *                       Pattern 2, relaxed, at exit; a cooperative grid.
  *  ARX_SYNC_PAD         triton_barrier.py's blockwise_barrier on the signal
  *                       pad for all three: Pattern 0 (relaxed) at the start,
  *                       Pattern 1 (acq_rel) after staging, Pattern 2

@@ -84,7 +84,7 @@ class Ctx:
         hdr = u32(0, 5)
         sem = host[c.off_sem: c.off_sem + 128 * W * B].reshape(W * B, 128)[:, :8].copy().view(np.uint32)
         return dict(seq=int(hdr[0]), err=int(hdr[1]), blocks=[int(hdr[2]), int(hdr[3])],
-                    published=int(hdr[4]), stagger=u32(128, 32).reshape(2, 16),
+                    published=int(hdr[4]), stagger=u32(128, 32),
                     epoch=u32(c.off_epoch, W * B).reshape(W, B),
                     flag=sem[:, 0].astype(np.int64).reshape(W, B),
                     counter=sem[:, 1].astype(np.int64).reshape(W, B),
@@ -104,9 +104,9 @@ class Ctx:
 
 
 def _stagger_groups(W, n, B):
-    """Block groups of a host-slot step: about 128 KiB of staged data each,
-    at most 16 and at most B; none below two (as include/arx.h describes)."""
-    K = min((W * n * 2 + (64 << 10)) >> 17, 16, B)
+    """Block groups of a host-slot step: about 128 KiB of staged data each, at
+    most B; none below two (as include/arx.h describes)."""
+    K = min((W * n * 2 + (64 << 10)) >> 17, B)
     return K if K >= 2 else 0
 
 
@@ -167,7 +167,8 @@ def test_host_slot_steps_of_varying_size(arx, dev):
     # Slots in host memory: steps of 192 KiB of partials or more stage in
     # turn, in a number of block groups that follows each step's size; smaller
     # ones all at once.  Mixing them on one context must not matter: every
-    # output bit-exact, the staging counts back to zero after every step.
+    # output bit-exact, the staggered step's start time back to zero after
+    # every step.
     W, max_n = 8, 131072
     c = Ctx(arx, dev, W, max_n, 0, "semaphore", "host")
     staggered = 0
@@ -328,8 +329,8 @@ def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync, slots):
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s}")
         _compare_to_model(c.words(), st)
     assert (c.words()["flag"] == (2 * W * k if sync in SEM_SYNCS else 0)).all()
-    # Staggered staging counts: zero between steps (the last block out of a
-    # staggered step clears its bank), host slots or not.
+    # Staggered staging's start time: zero between steps (the last block out
+    # of a staggered step clears it), host slots or not.
     assert not c.words()["stagger"].any()
     for r in range(W):
         assert np.array_equal(c.slot(k & 1, r, n), hist[k - 1][r])
