@@ -57,6 +57,8 @@ METRIC = "W-way bf16 reduce HBM GB/s ((W+1)·n·2 B / t); µs/call at bf16 [32,4
 DEFAULT_WORKLOAD = "w8_32x4096_normal"
 FALLBACK_HBM_GBS = 6800.0
 GRAPH_CALLS = 1000
+QUEUE_AHEAD_CYCLES = 400_000   # ~0.2 ms at 2 GHz: longer than submitting a graph replay
+LEAD_IN = 64                   # untimed calls at the head of the first timed graph (L2 turned over)
 ROTATE_FACTOR = 3          # rotation footprint >= this many L2 sizes
 
 
@@ -213,15 +215,23 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline object)
 
+ORACLE_WARM_S = 1.0   # untimed oracle calls before any timed ones (steady state)
+REF_STEP_S = 0.25     # length of one reference-arm step (repeated oracle calls)
+
+
 def time_oracle(W: int, n_sample: int, calls: int | None, budget_s: float, threads: int,
-                seed: int = 1, dist: str = "normal") -> dict:
-    """Times the oracle over ``n_sample`` elements drawn like the workload's partials."""
+                seed: int = 1, dist: str = "normal", warm_s: float = ORACLE_WARM_S) -> dict:
+    """Times the oracle over ``n_sample`` elements drawn like the workload's partials,
+    after ``warm_s`` seconds of untimed calls."""
     import oracle
     import synthetic_partials as sp
     x = sp.partials(W, n_sample, dist, seed)
     u = sp.to_u16_numpy(x)
     slots = list(u)
     out = oracle.reduce(slots, threads=threads)  # warm
+    t_warm = time.perf_counter()
+    while time.perf_counter() - t_warm < warm_s:
+        oracle.reduce(slots, out=out, threads=threads)
     done = 0
     t0 = time.perf_counter()
     while True:
@@ -235,6 +245,26 @@ def time_oracle(W: int, n_sample: int, calls: int | None, budget_s: float, threa
     return dict(calls=done, seconds=el, bytes=byts, gbs=byts / el / 1e9, threads=threads)
 
 
+def oracle_in_child(W: int, n: int, seconds: float, threads: int, seed: int, dist: str) -> dict:
+    """time_oracle in a fresh Python process that never initialises CUDA.
+
+    In a process whose CUDA context is up (with page-locked buffers
+    allocated), the oracle's per-call thread start-up measured about twice as
+    slow on the GB300 host as in a fresh process (16 threads: 2.4-2.5 against
+    5.2-5.8 GB/s, the same 1-thread rate): the baseline is taken where the
+    reference arm takes it, in a process of its own.
+    """
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.time_oracle(%d, %d, None, %r, %d, %d, %r)))"
+            % (ROOT, W, n, float(seconds), threads, seed, dist))
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=seconds * 4 + 120)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing child failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def run_reference(args) -> None:
     rank, world, _ = dist_env()
     if rank != 0:
@@ -244,23 +274,28 @@ def run_reference(args) -> None:
     spec = sp.WORKLOADS[args.workload]
     W, n = spec["W"], spec["n"] or args.n
     threads = oracle.default_threads()
-    # Bound the whole run to about two minutes of host time: each step reduces
-    # a contiguous sample of the workload's elements.
+    # Each step is the oracle over the workload (a contiguous sample of its
+    # elements where one call would take more than a second), repeated
+    # enough times that a step lasts about REF_STEP_S: a 20-step run then
+    # times seconds of steady-state calls, not a few milliseconds of them
+    # (the oracle starts its threads per call, and single calls vary).
     per_elem_s = 2.0e-9 * W / max(1, threads) + 1e-10
-    budget = 120.0
-    n_step = int(max(4096, min(n, budget / max(1, args.steps + args.warmup) / per_elem_s)))
-    n_step = min(n, n_step)
-    time_oracle(W, n_step, args.warmup, 0.0, threads, spec["seed"], spec["dist"])
-    r = time_oracle(W, n_step, args.steps, 0.0, threads, spec["seed"], spec["dist"])
+    n_step = int(min(n, max(4096, 1.0 / per_elem_s)))
+    calls = time_oracle(W, n_step, None, 0.5, threads, spec["seed"], spec["dist"])
+    reps = max(1, int(round(REF_STEP_S / (calls["seconds"] / calls["calls"]))))
+    time_oracle(W, n_step, args.warmup * reps, 0.0, threads, spec["seed"], spec["dist"], warm_s=0.0)
+    r = time_oracle(W, n_step, args.steps * reps, 0.0, threads, spec["seed"], spec["dist"])
     value = r["gbs"]
-    sample = (f"{args.steps} oracle calls, each over the first {n_step} of {n} elements of the "
-              f"{args.workload} partials (W={W}), {threads} threads")
+    sample = (f"{args.steps} steps of {reps} oracle calls each, every call over "
+              f"{'all' if n_step == n else f'the first {n_step} of'} {n} elements of the "
+              f"{args.workload} partials (W={W}), {threads} threads, after {args.warmup} warm-up steps "
+              f"and {ORACLE_WARM_S:.0f} s of untimed calls; a process without CUDA")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds"] / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "io_dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "W": W, "n": n, "n_per_step": n_step},
+        "config": {"workload": args.workload, "W": W, "n": n, "n_per_call": n_step, "calls_per_step": reps},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -279,10 +314,50 @@ def _graph_of_calls(torch, stream, fn, count):
     return g
 
 
+_FLUSH: dict = {}
+
+
+def flush_l2(torch, stream, l2_bytes: int) -> None:
+    """Evicts L2 with clean lines: reads a buffer of twice the L2 size on
+    ``stream`` (a read, so no dirty lines are left to write back later)."""
+    dev = torch.cuda.current_device()
+    buf = _FLUSH.get(dev)
+    if buf is None or buf.numel() < 2 * l2_bytes // 4:
+        buf = _FLUSH[dev] = torch.ones(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        buf.amax()
+
+
+def _timing_event(torch):
+    """A timing event that a CUDA graph can record inside itself (an external
+    event node), or None if this torch cannot make one."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
 def timed_graph_calls(torch, stream, fn, steps: int, warmup: int, chunk: int = GRAPH_CALLS,
                       sampler: ClockSampler | None = None) -> float:
-    """Seconds for exactly ``steps`` calls of fn(i), launched from CUDA graphs on ``stream``."""
+    """Seconds for exactly ``steps`` calls of fn(i), launched from CUDA graphs on ``stream``.
+
+    The start and end events are recorded by the graphs themselves.  The
+    first graph opens with LEAD_IN untimed calls (the last of the warm-up
+    calls), and the start event fires when the last of them completes; the
+    end event fires when the last timed call completes, and LEAD_IN untimed
+    calls follow it.  The timed region is thus exactly ``steps`` call
+    completions of a running stream of calls -- each call overlaps its
+    predecessor's tail (programmatic dependent launch), as in a long run --
+    and neither the host's submission of the replay nor the GPU's launch of
+    the graph falls inside it.  Before the
+    timed replays L2 is flushed (the warm-up replays touched the same
+    buffers), so a short run's calls read their inputs from DRAM like a long
+    run's.  Without graph-recordable events (older torch) the events are
+    recorded on the stream around the replays instead.
+    """
     chunk = max(1, min(chunk, steps))
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
     # Inputs, outputs and zero-filled workspaces were made on torch's default
     # stream; `stream` is a non-blocking stream, so order them before its calls.
     torch.cuda.synchronize()
@@ -290,28 +365,70 @@ def timed_graph_calls(torch, stream, fn, steps: int, warmup: int, chunk: int = G
         for i in range(max(1, min(warmup, 8))):   # eager warm-up (launch caches, lazy init)
             fn(i)
     torch.cuda.synchronize()
-    g_full = _graph_of_calls(torch, stream, fn, chunk)
-    rem = steps % chunk
-    g_rem = _graph_of_calls(torch, stream, lambda i: fn(steps - rem + i), rem) if rem else None
+    start, end = _timing_event(torch), _timing_event(torch)
+    in_graph = start is not None and end is not None
+    if not in_graph:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+    side, side2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def capture(count, base, first, last):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if first and in_graph:
+                for i in range(LEAD_IN):    # untimed: the stream of calls is running
+                    fn(steps + i)
+                side.wait_stream(stream)     # fires when the last lead-in call completes
+                start.record(side)
+            for i in range(count):
+                fn(base + i)
+            if last and in_graph:
+                # The end event on a branch of its own, like the start event,
+                # followed by untimed calls: both events are recorded while
+                # the GPU is still launching calls, so any delay in recording
+                # them is alike at both ends.
+                side2.wait_stream(stream)    # fires when the last timed call completes
+                end.record(side2)
+                for i in range(LEAD_IN):
+                    fn(steps + LEAD_IN + i)
+            if first and in_graph:
+                stream.wait_stream(side)
+            if last and in_graph:
+                stream.wait_stream(side2)
+        return g
+
+    segs = [chunk] * (steps // chunk) + ([steps % chunk] if steps % chunk else [])
+    if len(segs) == 1:
+        order = [capture(segs[0], 0, True, True)]
+    else:
+        g_first = capture(segs[0], 0, True, False)
+        g_mid = capture(chunk, 0, False, False) if len(segs) > 2 else None
+        g_last = capture(segs[-1], steps - segs[-1], False, True)
+        order = [g_first] + [g_mid] * (len(segs) - 2) + [g_last]
     # CUDAGraph.replay() launches on torch's current stream: make it `stream`,
     # the stream the events are recorded on.
     with torch.cuda.stream(stream):
-        # Warm-up replays (untimed): at least `warmup` calls.
-        for _ in range(max(1, (warmup + chunk - 1) // chunk)):
-            g_full.replay()
+        # Warm-up replays (untimed): every graph once (its first launch
+        # uploads it), then the full chunk until `warmup` calls have run.
+        for g in dict.fromkeys(order):
+            g.replay()
+        for _ in range(max(0, (warmup - steps + chunk - 1) // chunk)):
+            order[0].replay()
         torch.cuda.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
         if sampler:
             sampler.mark_start()
-        start.record(stream)
-        for _ in range(steps // chunk):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
+        flush_l2(torch, stream, l2)
+        # A bounded spin, off the clock, keeps the GPU busy while the host
+        # submits the replays, so they run back to back.
+        torch.cuda._sleep(QUEUE_AHEAD_CYCLES)
+        if not in_graph:
+            start.record(stream)
+        for g in order:
+            g.replay()
+        if not in_graph:
+            end.record(stream)
         torch.cuda.synchronize()
     if sampler:
         sampler.mark_end()
@@ -380,11 +497,16 @@ def run_native(args) -> None:
         extra["hot_l2"] = hot_l2_point(torch, arx, stream, slot_lists, outs, W, n)
         extra["stream_launch"] = stream_launch_point(torch, arx, dev, stream, slot_lists, outs, R)
         extra["bandwidth"] = bandwidth_points(torch, arx, sp, dev, stream, l2)
+        extra["sweep"] = {"workload": "w8_sweep_int values (integers in [-8, 8]) at W = 2, 4, 8",
+                          "peak_GBs": measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS,
+                          "points": {f"W{w}": sweep_points(torch, arx, dev, stream, l2, w, SWEEP_LOG2)
+                                     for w in SWEEP_W}}
         extra["protocol"] = protocol_point(torch, arx, sp, dev, stream, l2, args.workload)
         extra["protocol_graph"] = protocol_graph_point(torch, arx, sp, dev, stream)
         link = pinned_copy_gbs(torch, dev)
         extra["protocol_host_slots"] = protocol_host_slots_point(torch, arx, sp, dev, stream, l2,
                                                                  args.workload, link)
+        extra["external_writer"] = ext_point(torch, arx, sp, dev, stream, args.workload, link)
         extra["e2e"] = e2e_point(torch, arx, sp, dev, stream, args.workload, max(200, min(args.steps, 5000)),
                                  l2, link)
     if rank != 0:
@@ -399,13 +521,15 @@ def run_native(args) -> None:
     if not args.no_cpu_baseline:
         import oracle
         threads = oracle.default_threads()
-        r = time_oracle(W, n, None, args.cpu_seconds, threads, spec["seed"], spec["dist"])
+        r = oracle_in_child(W, n, args.cpu_seconds, threads, spec["seed"], spec["dist"])
         cpu = {"value": r["gbs"], "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{r['calls']} full calls of the {args.workload} workload "
-                         f"(W={W}, n={n}) in {r['seconds']:.1f} s on {threads} host threads"}
-        r1 = time_oracle(W, n, None, args.cpu_seconds / 2, 1, spec["seed"], spec["dist"])
+                         f"(W={W}, n={n}) in {r['seconds']:.1f} s on {threads} host threads, after "
+                         f"{ORACLE_WARM_S:.0f} s of untimed calls, in a child process without CUDA"}
+        r1 = oracle_in_child(W, n, args.cpu_seconds / 2, 1, spec["seed"], spec["dist"])
         cpu1 = {"value": r1["gbs"], "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"{r1['calls']} full calls in {r1['seconds']:.1f} s on 1 host thread"}
+                "sample": f"{r1['calls']} full calls in {r1['seconds']:.1f} s on 1 host thread, "
+                          f"in a child process without CUDA"}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
@@ -513,13 +637,14 @@ def floor_point(torch, arx, dev, stream, l2, W, n, per_call) -> dict:
             "marginal_GBs": gbs((W + 1) * n * 2, above) if above > 0 else None}
 
 
-SYNC_MODES = ("semaphore", "pad", "pad_fenced", "cluster")
+SYNC_MODES = ("semaphore", "pad", "pad_fenced", "cluster", "semaphore_global")   # index = ARX_SYNC_*
 
 
 def protocol_point(torch, arx, sp, dev, stream, l2, workload, steps: int = 2000) -> dict:
     """arx_step per step (W=8, [32,4096]) in captured graphs, fresh input sets rotating,
-    for each barrier variant (Semaphore barriers; pad barrier Patterns 0/1/2; all acq_rel;
-    the thread-block cluster barrier)."""
+    for each barrier variant (Semaphore barriers with the flags in the cluster's shared
+    memory; pad barrier Patterns 0/1/2; all acq_rel; the thread-block cluster barrier;
+    Semaphore barriers with the flags in global memory)."""
     W, n = 8, sp.N_32x4096
     x, _ = sp.workload(workload)
     R = rotation_sets(W * n * 2 * 2, l2)
@@ -614,6 +739,7 @@ def protocol_graph_point(torch, arx, sp, dev, stream) -> dict:
             for _ in range(3):
                 s = torch.cuda.Event(enable_timing=True)
                 e = torch.cuda.Event(enable_timing=True)
+                torch.cuda._sleep(QUEUE_AHEAD_CYCLES)   # replay queued when s fires
                 s.record(stream)
                 g.replay()
                 e.record(stream)
@@ -667,6 +793,74 @@ def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link, s
                                   "both directions at once (the steps stage in turn, so writes and "
                                   "reads overlap)",
                          "serial_bound_us": t_serial * 1e6, "serial_frac": t_serial / t}}
+
+
+def ext_point(torch, arx, sp, dev, stream, workload, link, steps: int = 1000, warm: int = 20) -> dict:
+    """The external-writer form: a host thread (standing in for arx.cu's proxy
+    and NIC) raises the W flags of every step, the GPU waits for them and
+    reduces the W page-locked slots over NVLink-C2C.  The slots of both banks
+    hold the workload's partials, written once in place (arx_ext_slot), so the
+    producer only publishes (arx_ext_publish_all, which first waits for the
+    bank to be free); this times the GPU side of the hand-off.  ``steps``
+    steps in one CUDA graph, the events recorded by the graph.  Link
+    roofline: W*n*2 bytes read over the link per step at the measured pinned
+    host->device copy rate."""
+    import ctypes
+    import threading
+    W, n = 8, sp.N_32x4096
+    x, _ = sp.workload(workload)
+    words = torch.zeros(arx.arx_ext_words_bytes(), dtype=torch.uint8, device=dev)
+    region = torch.zeros(arx.arx_ext_region_bytes(W, n), dtype=torch.uint8).pin_memory()
+    xe = arx.arx_ext_init(words, region, W, n)
+    arx.arx_ext_set_timeout(xe, 50_000_000)   # a stalled producer costs 50 ms per step, not 1 s
+    for par in (0, 1):
+        for r in range(W):
+            ctypes.memmove(arx.arx_ext_slot(xe, par, r), x[r].data_ptr(), n * 2)
+    out = torch.empty(steps, n, dtype=torch.bfloat16, device=dev)
+    errors = []
+
+    def producer(total):
+        try:
+            for s_ in range(1, total + 1):
+                arx.arx_ext_publish_all(xe, s_, wait_s=20.0)
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    start, end = _timing_event(torch), _timing_event(torch)
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        side.wait_stream(stream)
+        start.record(side)
+        for i in range(steps):
+            arx.arx_ext_step(xe, out[i], stream=stream)
+        end.record(stream)
+        stream.wait_stream(side)
+    th = threading.Thread(target=producer, args=(warm + 2 * steps,))
+    th.start()
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            arx.arx_ext_step(xe, out[i], stream=stream)
+        g.replay()                      # warm-up replay (uploads the graph)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(QUEUE_AHEAD_CYCLES)
+        g.replay()
+        torch.cuda.synchronize()
+    th.join()
+    t = start.elapsed_time(end) / 1e3 / steps
+    st, seq, err = arx.arx_ext_query(xe, stream=stream)
+    import oracle
+    want = oracle.reduce(list(sp.to_u16_numpy(x)))
+    ok = bool((sp.to_u16_numpy(out[steps - 1].cpu()) == want).all())
+    moved = W * n * 2
+    peak = link["h2d"]
+    return {"W": W, "n": n, "steps": steps, "blocks": xe.nblocks, "us_per_step": t * 1e6,
+            "status": arx.arx_status_string(st), "seq": seq, "dev_err": err, "producer_errors": errors,
+            "bit_exact": ok, "metric_GBs": gbs((W + 1) * n * 2, t),
+            "roofline": {"bound": "c2c", "achieved": gbs(moved, t), "peak": peak, "unit": "GB/s",
+                         "frac": gbs(moved, t) / peak,
+                         "basis": "W*n*2 bytes of slots read over the link per step, against the measured "
+                                  "pinned host->device copy rate"}}
 
 
 def pinned_copy_gbs(torch, dev, nbytes: int = 1 << 26, reps: int = 5) -> dict:
@@ -845,24 +1039,15 @@ def e2e_point(torch, arx, sp, dev, stream, workload, steps, l2, link) -> dict:
                                          "sum copied back, same buffers and graphs"}}
 
 
-def run_sweep(args) -> None:
-    """GB/s vs per-partial size for the integer sweep workload (W = 8, n = 2^9 .. 2^27).
-
-    Same timing method as the headline (graph replays, rotation footprint
-    above 3x L2).  Values are drawn on the device (timing only; parity at every
-    size is in the tests).  Prints one JSON object.
-    """
-    import torch
-    import deterministic_shot_all_gb300 as arx
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
-    stream = torch.cuda.Stream(device=dev)
+def sweep_points(torch, arx, dev, stream, l2, W: int, log2_sizes) -> list:
+    """GB/s of arx_reduce against size for the integer sweep workload (W partials
+    of 2^k elements, k in ``log2_sizes``), by the headline's method (graph
+    replays, rotation footprint above 3x L2, L2 flushed before the timed
+    calls).  Values are drawn on the device (timing only; parity at every size
+    is in the tests)."""
     peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
-    W = args.sweep_w
     pts = []
-    for k in range(args.sweep_min, args.sweep_max + 1):
+    for k in log2_sizes:
         n = 1 << k
         set_bytes = (W + 1) * n * 2
         R = rotation_sets(set_bytes, l2)
@@ -881,7 +1066,26 @@ def run_sweep(args) -> None:
                     "us_per_call": t / calls * 1e6, "GBs": g, "frac": g / peak})
         del parts, outs, lists
         torch.cuda.empty_cache()
-    print(json.dumps({"sweep": "arx_reduce", "W": W, "peak_GBs": peak,
+    return pts
+
+
+SWEEP_W = (2, 4, 8)
+SWEEP_LOG2 = (19, 20, 21, 22, 23)     # 1 MiB .. 16 MiB per partial
+
+
+def run_sweep(args) -> None:
+    """GB/s vs per-partial size for the integer sweep workload (W = --sweep-w,
+    n = 2^--sweep-min .. 2^--sweep-max); prints one JSON object."""
+    import torch
+    import deterministic_shot_all_gb300 as arx
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    stream = torch.cuda.Stream(device=dev)
+    peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+    pts = sweep_points(torch, arx, dev, stream, l2, args.sweep_w, range(args.sweep_min, args.sweep_max + 1))
+    print(json.dumps({"sweep": "arx_reduce", "W": args.sweep_w, "peak_GBs": peak,
                       "peak_source": "of measured" if measured_peaks().get("hbm_gbs") else "of fallback",
                       "points": pts}), flush=True)
 
@@ -916,6 +1120,20 @@ def run_protocol_host(args) -> None:
     print(json.dumps({"protocol_host_slots": res, "link": link}), flush=True)
 
 
+def run_ext(args) -> None:
+    """Only the external-writer step (W = 8 bf16 [32, 4096], --steps steps in one
+    graph); prints one JSON object.  Used to profile its kernel."""
+    import torch
+    import deterministic_shot_all_gb300 as arx
+    import synthetic_partials as sp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    link = pinned_copy_gbs(torch, dev)
+    res = ext_point(torch, arx, sp, dev, stream, DEFAULT_WORKLOAD, link, steps=args.steps)
+    print(json.dumps({"external_writer": res, "link": link}), flush=True)
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -936,6 +1154,8 @@ def main(argv=None) -> None:
     p.add_argument("--protocol", action="store_true", help="only the protocol step, every barrier variant")
     p.add_argument("--protocol-host", action="store_true",
                    help="only the protocol step with its slots in page-locked host memory")
+    p.add_argument("--ext", action="store_true",
+                   help="only the external-writer step (host producer, GPU consumer)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -947,6 +1167,8 @@ def main(argv=None) -> None:
         run_protocol(args)
     elif args.protocol_host:
         run_protocol_host(args)
+    elif args.ext:
+        run_ext(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
