@@ -520,7 +520,9 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     __syncwarp();
     cluster_wait();
     if (tid == owner) {
-      if (shared_semaphore_wait<false>(flag_sh, base, uint32_t(W), a.timeout_ns)) {
+      // flag - counter = (flag_in + W + adds) - (flag_in + base): the page's
+      // unsigned test flag - counter >= 2W is adds - (base - W) >= 2W.
+      if (shared_semaphore_wait<false>(flag_sh, base - uint32_t(W), 2u * uint32_t(W), a.timeout_ns)) {
         base += 2u * uint32_t(W);  // the counter after this step
       } else {
         record_error(&hdr->err, kErrTimeout, kEndWait, r, b);

@@ -152,3 +152,28 @@ def test_cluster_mode_has_no_signal_to_skip():
 def test_unknown_mode_is_rejected():
     with pytest.raises(ValueError):
         P.step(P.State(W=1, B=1), _inputs(1, 8, 0), sync="fenced")
+
+
+@pytest.mark.parametrize("W,B,k", [(1, 1, 2), (3, 2, 3), (8, 4, 5)])
+def test_semaphore_global_mode_closed_form(W, B, k):
+    # Where the GPU holds a Semaphore flag during the step (global memory, or
+    # the shared memory of a thread-block cluster) does not change
+    # PullController::sync's arithmetic: after k steps flag == counter == 2Wk,
+    # the pad is all zero, the epoch is k mod 2 -- as in the default mode.
+    st = P.State(W=W, B=B)
+    for s in range(k):
+        x = _inputs(W, 64, s)
+        assert np.array_equal(P.step(st, x, sync="semaphore_global"), oracle.reduce(x))
+    assert (st.flag == 2 * W * k).all() and (st.counter == 2 * W * k).all()
+    assert not st.pad.any() and (st.epoch == k % 2).all() and st.seq == k and st.err == 0
+
+
+def test_semaphore_global_missing_end_signal_reports_timeout():
+    # One rank skips its end signal: every flag gets 2W - 1 adds, no counter
+    # advances, and the error word reports ETIMEOUT -- the same words as the
+    # default mode's.
+    W, B = 4, 2
+    st = P.State(W=W, B=B)
+    P.step(st, _inputs(W, 32, 0), skip_end_signal_rank=1, sync="semaphore_global")
+    assert st.err == P.ETIMEOUT
+    assert (st.flag == 2 * W - 1).all() and (st.counter == 0).all()
