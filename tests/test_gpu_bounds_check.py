@@ -1,8 +1,8 @@
 """Random cases through the bounds-checking build of the library.
 
 ``libarx_boundscheck.so`` is the same library built with ``ARX_BOUNDS_CHECK``:
-every data access of the reduce and step kernels (partials, slots, output)
-is first checked against the buffer it belongs to; a failed check is counted
+every data access of the reduce, step and external-writer kernels (partials,
+slots, output) is first checked against the buffer it belongs to; a failed check is counted
 and the access skipped.  With compute-sanitizer unavailable, this stands in
 for an out-of-bounds detector: random shapes, offsets, aliasing, block counts
 and barrier variants must give the oracle's bits with a counter of zero.  A
@@ -44,6 +44,13 @@ def checked(arx):
             ("arx_step", [ctxp, ptrs, vp, sz, vp], i32),
             ("arx_bounds_violations", [ctypes.POINTER(ctypes.c_uint32), i32], i32),
             ("arx_bounds_probe", [vp], i32),
+            ("arx_ext_region_bytes", [i32, sz], sz),
+            ("arx_ext_words_bytes", [], sz),
+            ("arx_ext_init", [ctypes.POINTER(arx.arx_ext), vp, sz, vp, sz, i32, sz, i32], i32),
+            ("arx_ext_post", [ctypes.POINTER(arx.arx_ext), i32, ctypes.c_uint32, vp, sz, ctypes.c_uint64], i32),
+            ("arx_ext_step", [ctypes.POINTER(arx.arx_ext), vp, sz, vp], i32),
+            ("arx_ext_query", [ctypes.POINTER(arx.arx_ext), ctypes.POINTER(ctypes.c_uint32),
+                               ctypes.POINTER(ctypes.c_uint32), vp], i32),
             ("arx_last_error", [], ctypes.c_char_p)):
         fn = getattr(L, name)
         fn.argtypes = args
@@ -134,4 +141,36 @@ def test_random_steps_stay_in_bounds(checked, arx):
                               f"case {case} step {s}: W={W} n={n} B={ctx.nblocks} mode={mode}")
         words = ws[:8].cpu().numpy().view(np.uint32)
         assert words[0] == 2 and words[1] == 0, f"case {case}: seq {words[0]} err {words[1]:#x}"
+    assert _violations(checked) == 0
+
+
+def test_random_external_writer_steps_stay_in_bounds(checked, arx):
+    # The external-writer kernel through the checking build: random W, ragged
+    # n (slots of a larger max_n) and output offsets, two steps each (both
+    # banks), outputs against the oracle and no access outside its buffer.
+    dev = torch.device("cuda:0")
+    _violations(checked)
+    rng = np.random.default_rng(7171)
+    for case in range(20):
+        W = int(rng.integers(1, 9))
+        max_n = int(rng.integers(1, 70000))
+        n = int(rng.integers(1, max_n + 1))
+        off = int(rng.integers(0, 8))
+        words = torch.zeros(checked.arx_ext_words_bytes(), dtype=torch.uint8, device=dev)
+        region = torch.zeros(checked.arx_ext_region_bytes(W, max_n), dtype=torch.uint8).pin_memory()
+        x = arx.arx_ext()
+        assert checked.arx_ext_init(ctypes.byref(x), words.data_ptr(), words.numel(), region.data_ptr(),
+                                    region.numel(), W, max_n, 0) == 0, checked.arx_last_error()
+        ob = torch.zeros(n + 16, dtype=torch.int16, device=dev)
+        out = ob[off:off + n]
+        for s in (1, 2):
+            p = sp.partials(W, n, "special", seed=71_000 + 2 * case + s)
+            for r in range(W):
+                assert checked.arx_ext_post(ctypes.byref(x), r, s, p[r].data_ptr(), n, 10**9) == 0
+            assert checked.arx_ext_step(ctypes.byref(x), out.data_ptr(), n, _stream()) == 0
+            seq, err = ctypes.c_uint32(0), ctypes.c_uint32(0)
+            assert checked.arx_ext_query(ctypes.byref(x), ctypes.byref(seq), ctypes.byref(err), _stream()) == 0
+            assert (seq.value, err.value) == (s, 0)
+            assert_bits_equal(out.cpu().numpy().view(np.uint16), oracle.reduce(list(sp.to_u16_numpy(p))),
+                              f"case {case} step {s}: W={W} n={n} max_n={max_n} off={off}")
     assert _violations(checked) == 0
