@@ -12,14 +12,21 @@ Timing rules followed:
   enough buffer sets that their footprint is more than 3x the L2, so no call
   finds its inputs in L2 (stated in ``config``);
 * >= 3 untimed warm-up steps, then exactly K timed steps, all launched from
-  CUDA graphs (captured off the clock) on one stream and bracketed by CUDA
-  events recorded on that stream, with a barrier and a device synchronise on
-  both sides; the maximum over ranks is reported;
+  CUDA graphs (captured off the clock) on one stream; the timing events are
+  recorded by the graphs themselves, the start one when the last of 64
+  untimed lead-in calls completes and the end one when the last timed call
+  completes (64 untimed calls follow), so the region holds exactly K call
+  completions of a running stream of calls; L2 is flushed before the timed
+  replay; a barrier and a device synchronise on both sides; the maximum over
+  ranks is reported;
 * nvidia-smi clocks and throttle reasons are sampled around the timed region.
 
 Extra objects on the one JSON line: ``roofline`` (the reduce kernel against
 the measured HBM copy bandwidth), ``cpu_baseline`` / ``cpu_baseline_1thread``
-(the CPU oracle on all host cores and on one, bounded samples), ``e2e`` (the
+(the CPU oracle on all host cores and on one, bounded samples, timed in a
+child process without CUDA), ``sweep`` (GB/s against size at W = 2, 4, 8),
+``external_writer`` (a host thread raises the flags, the GPU reduces the
+page-locked slots), ``e2e`` (the
 same metric through ``arx_reduce_host`` with pinned host buffers, the
 partials crossing the CPU-GPU link every call, against the link's measured
 pinned copy rate), ``bandwidth`` (bandwidth-bound sizes: W=4 [1024, 8192] in
@@ -537,8 +544,12 @@ def run_native(args) -> None:
         "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "W": W, "n": n, "shape": [32, 4096] if n == 32 * 4096 else [n],
                    "out_aliases_slot0": alias, "l2": f"inputs rotate over {R} buffer sets "
-                   f"({R * set_bytes / 1e6:.0f} MB > {ROTATE_FACTOR}x L2 {l2 / 1e6:.0f} MB)",
-                   "launch": f"CUDA graphs of {min(GRAPH_CALLS, args.steps)} arx_reduce calls, replayed",
+                   f"({R * set_bytes / 1e6:.0f} MB > {ROTATE_FACTOR}x L2 {l2 / 1e6:.0f} MB); "
+                   f"L2 flushed (a read of 2x its size) before the timed replay",
+                   "launch": f"CUDA graphs of up to {GRAPH_CALLS} arx_reduce calls, replayed; the first "
+                             f"graph opens with {LEAD_IN} untimed calls and the last closes with "
+                             f"{LEAD_IN}; start and end events recorded by the graphs when the last "
+                             f"untimed call before and the last timed call complete",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic,
