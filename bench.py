@@ -796,6 +796,18 @@ def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link, s
     moved = W * n * 2
     t_serial = moved / (link["d2h"] * 1e9) + moved / (link["h2d"] * 1e9)
     t_duplex = 2 * moved / (link["both"] * 1e9)
+    # The same step on the thread-block cluster barrier (no Semaphore words,
+    # no fault knob): the fastest host-slot form.
+    words_c = torch.zeros(arx.arx_ctx_words_bytes(W), dtype=torch.uint8, device=dev)
+    slots_c = torch.empty(arx.arx_ctx_slots_bytes(W, n), dtype=torch.uint8).pin_memory()
+    ctx_c = arx.arx_ctx_init_split(words_c, slots_c, W, n)
+    arx.arx_ctx_set_sync(ctx_c, arx.ARX_SYNC_CLUSTER)
+
+    def call_c(i):
+        arx.arx_step(ctx_c, lists[i % R], outs[i % R], stream=stream)
+
+    tc = timed_graph_calls(torch, stream, call_c, steps, 10) / steps
+    stc, seqc, _ = arx.arx_ctx_query(ctx_c, stream=stream)
     return {"W": W, "n": n, "steps": steps, "blocks_per_rank": ctx.nblocks, "us_per_step": t * 1e6,
             "status": arx.arx_status_string(st), "seq": seq,
             "link_bytes_per_step": 2 * moved,
@@ -803,7 +815,9 @@ def protocol_host_slots_point(torch, arx, sp, dev, stream, l2, workload, link, s
                          "basis": "staged bytes out and back at the measured rate of pinned copies in "
                                   "both directions at once (the steps stage in turn, so writes and "
                                   "reads overlap)",
-                         "serial_bound_us": t_serial * 1e6, "serial_frac": t_serial / t}}
+                         "serial_bound_us": t_serial * 1e6, "serial_frac": t_serial / t},
+            "cluster": {"us_per_step": tc * 1e6, "frac": t_duplex / tc, "status": arx.arx_status_string(stc),
+                        "seq": seqc}}
 
 
 def ext_point(torch, arx, sp, dev, stream, workload, link, steps: int = 1000, warm: int = 20) -> dict:

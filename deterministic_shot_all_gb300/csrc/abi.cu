@@ -504,9 +504,7 @@ arx_status arx_step(const arx_ctx* ctx, const void* const* inputs, void* out, si
   c.B = ctx->nblocks;
   c.fault_rank = ctx->fault_rank;
   c.sync_mode = ctx->sync_mode;
-  c.stagger = ctx->slots_where == ARX_SLOTS_HOST && ctx->sync_mode != ARX_SYNC_CLUSTER
-                  ? stagger_groups(ctx->W, n, ctx->nblocks)
-                  : 0;
+  c.stagger = ctx->slots_where == ARX_SLOTS_HOST ? stagger_groups(ctx->W, n, ctx->nblocks) : 0;
   c.stagger_ns = stagger_ns(ctx->W, n, c.stagger);
   ARX_SET_BOUNDS_COUNTER(c);
   e = arx::launch_step(c, static_cast<cudaStream_t>(stream));

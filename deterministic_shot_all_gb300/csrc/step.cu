@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   constexpr bool kDsm = kSync == kSyncSemaphore;    // clusters too; Semaphores in shared memory
   constexpr bool kSemGlobal = kSync == kSyncSemaphoreGlobal;
   constexpr bool kFencedAll = kSync == kSyncPadFenced;
-  static_assert(!(kStagger && (kCluster || kDsm)), "the cluster-launched variants stage all at once");
+  static_assert(!(kStagger && kDsm), "host-slot steps stagger with the Semaphores in global memory");
   const uint32_t b = blockIdx.x, r = blockIdx.y;
   const uint32_t B = uint32_t(a.B);
   const uint32_t tid = threadIdx.x, warp = tid / 32u, lane = tid % 32u;
@@ -653,7 +653,8 @@ int blocks_per_sm(int dev, cudaError_t* err) {
     if (c > 0) return c;
   }
   int lo = 0;
-  const void* kernels[8] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+  const void* kernels[9] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, true>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
@@ -749,10 +750,12 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
                : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncPadFenced, false>, a);
       break;
     case kSyncCluster:
-      // No staggered staging in this variant (arx_step passes none).
+      // The staggered staging waits for no other block, so the clusters
+      // need not be co-resident in this variant either.
       cfg.attrs = cattr;
       cfg.numAttrs = 2;
-      err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncCluster, false>, a);
+      err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncCluster, true>, a)
+               : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncCluster, false>, a);
       break;
     default: break;
   }
@@ -784,8 +787,9 @@ int cluster_capacity_w(cudaError_t* err) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int lo = 0;
-  const void* kernels[2] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>)};
+  const void* kernels[3] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, true>)};
   for (const void* k : kernels) {
     int c = 0;
     *err = cudaOccupancyMaxActiveClusters(&c, k, &cfg);

@@ -286,8 +286,9 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
  *                       and the fault-injection knob, which would make a
  *                       block skip an arrival, is refused (ARX_EINVAL).  So
  *                       "every wait is bounded" holds in this mode only in
- *                       that sense.  Slots in host memory are staged all at
- *                       once.
+ *                       that sense.  Slots in host memory are staged in
+ *                       turn, as in the flag modes (the fastest host-slot
+ *                       step).
  * After every completed step the pad is all zero in every mode; in the pad
  * and cluster modes the Semaphore flags and counters keep their values.
  * Every mode may be selected on any context: the co-residency limit that
