@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     // this wait returns -- counted into the flag as W at write-back.  The
     // owner's warp arrives with release, so the zeroed word is in place
     // before any peer's add can reach it; the other warps arrive relaxed (a
-    // release arrival by every warp measured 2-4 % slower).  The global words
+    // release arrival by every warp measured about 2 % slower).  The global words
     // are loaded between arrival and wait and first used at the end stage,
     // so their latency hides behind the barrier and the staging.
     __syncwarp();  // the cluster barrier instructions are warp-aligned
