@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // to it through distributed shared memory.  The counter is read and
   // written only by its owner, so it stays in a register (`base`).
   __shared__ uint32_t s_sem_flag;
+  __shared__ uint2 s_words;  // the block's (flag, counter) as the previous step left them
   const uint32_t flag_sh = shared_address(&s_sem_flag);
   const uint32_t owner = 32u * r;  // warp r, lane 0: the thread that waits on this block's flag
 
@@ -319,10 +320,15 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   }
   dependent_launch_prologue();
 
-  // 1. seq / parity; epoch check (both words loaded back to back).
+  // 1. seq / parity; epoch check (the words loaded back to back).  In the
+  // Semaphore variant tid 0 also loads the block's Semaphore words in the
+  // same round trip and hands them to the owner through shared memory: 4.0
+  // against 4.2 us per step with the owner loading them itself between its
+  // start arrival and wait (W = 8 [32, 4096], A/B in one process, GB300).
   if (tid == 0) {
     const uint32_t done = ld_relaxed_gpu(&hdr->seq);
     const uint32_t epoch_in = epoch[r * B + b];
+    if constexpr (kDsm) s_words = *reinterpret_cast<const uint2*>(&sem[r * B + b]);
     const uint32_t seq = done + 1u;
     s_seq = seq;
     s_epoch = epoch_in;
@@ -359,15 +365,9 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     // this wait returns -- counted into the flag as W at write-back.  The
     // owner's warp arrives with release, so the zeroed word is in place
     // before any peer's add can reach it; the other warps arrive relaxed (a
-    // release arrival by every warp measured about 2 % slower).  The global words
-    // are loaded between arrival and wait and first used at the end stage,
-    // so their latency hides behind the barrier and the staging.
+    // release arrival by every warp measured about 2 % slower).
     __syncwarp();  // the cluster barrier instructions are warp-aligned
     if (warp == r) cluster_arrive_release(); else cluster_arrive_relaxed();
-    if (tid == owner) {
-      flag_in = own.flag;
-      base = own.counter - flag_in;
-    }
     __syncwarp();
     cluster_wait();
   } else if constexpr (kCluster) {
@@ -391,6 +391,12 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
                               kStartPadSend, kStartPadWait);
   }
   __syncthreads();
+  if constexpr (kDsm) {
+    if (tid == owner) {
+      flag_in = s_words.x;
+      base = s_words.y - flag_in;
+    }
+  }
   const uint32_t seq = s_seq;
   const uint32_t par = seq & 1u;
   const size_t stride = size_t(a.slot_stride);
@@ -502,7 +508,9 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     // it passes at once unless a signal is missing (the fault knob), in
     // which case it waits, bounded, and reports ARX_ETIMEOUT -- and advances
     // the counter.  Measured (W = 8 [32, 4096], GB300, A/B of library builds
-    // in one process): 4.1 us per step with this form; 4.4-4.5 us with the
+    // in one process): 4.0 us per step with this form (a build without the
+    // adds and the check, which cannot count a missing signal, was no
+    // faster); 4.4-4.5 us with the
     // owner polling its flag for release adds and no hardware barrier after
     // staging, 4.6 us with the adds issued after the arrival (the check then
     // waits for them, and an exit barrier must keep them from landing in an
@@ -527,6 +535,14 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       } else {
         record_error(&hdr->err, kErrTimeout, kEndWait, r, b);
       }
+      // Write the step's Semaphore words back (common.cuh keeps them in
+      // memory between calls): the flag with every signal of the step
+      // counted (W at the start barrier, the landed end-stage adds), the
+      // counter advanced by 2W after a successful end stage.  Stored here,
+      // where every add has landed, so the stores overlap the reduce: 4.19
+      // against 4.27 us per step storing them at the block's exit.
+      own.flag = flag_in + uint32_t(W) + ld_relaxed_cluster_shared(flag_sh);
+      own.counter = base + flag_in;
     }
   } else if (lane == 0 && warp < uint32_t(W)) {
     if (int(r) != a.fault_rank) {
@@ -627,16 +643,6 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     // always ends.
     __syncwarp();
     cluster_wait();
-  }
-  if constexpr (kDsm) {
-    // Write the step's Semaphore words back (common.cuh keeps them in memory
-    // between calls): the flag with every signal of the step counted (W at
-    // the start barrier, the landed end-stage adds), the counter advanced by
-    // 2W after a successful end stage.
-    if (tid == owner) {
-      own.flag = flag_in + uint32_t(W) + ld_relaxed_cluster_shared(flag_sh);
-      own.counter = base + flag_in;
-    }
   }
 }
 
