@@ -34,7 +34,7 @@
 //    (release arrival, acquire wait) orders the staged slots and the adds;
 //    the owner then checks flag - counter >= 2W, bounded, which waits only
 //    if a signal is missing.  The flag and counter are loaded at entry and
-//    written back at exit, so the words in memory follow the same
+//    written back after that check, so the words in memory follow the same
 //    arithmetic.  No add is in flight after the end barrier, so no exit
 //    barrier is needed; the kernel boundary stands in for Pattern 2 (the
 //    next kernel on the stream starts only after every block of this one
@@ -318,6 +318,21 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     const size_t bytes = (c1 - c0) * 16u < kPrefetchBytes ? (c1 - c0) * 16u : kPrefetchBytes;
     ARX_CHECKED(s4 + c0, bytes, a.in[r], a.n * 2, a.bounds_counter, prefetch_l2_bulk(s4 + c0, uint32_t(bytes)));
   }
+  if constexpr (kDsm) {
+    // The owner zeroes its flag (the shared word counts this step's
+    // end-stage adds from zero) and its warp arrives at the start barrier
+    // with release, which puts the zero in place before any peer's add can
+    // reach it.  Done before the dependency wait -- shared memory and the
+    // cluster barrier belong to this launch alone -- so the release, about
+    // 0.3 us, overlaps that wait: 3.76 against 4.0 us per step with the
+    // owner's warp arriving after its first staging loads (W = 8
+    // [32, 4096], A/B in one process, GB300).
+    if (tid == owner) st_shared(flag_sh, 0u);
+    if (warp == r) {
+      __syncwarp();  // the cluster barrier instructions are warp-aligned
+      cluster_arrive_release();
+    }
+  }
   dependent_launch_prologue();
 
   // 1. seq / parity; epoch check (the words loaded back to back).  In the
@@ -337,13 +352,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   Semaphore& own = sem[r * B + b];
   uint32_t base = 0;
   uint32_t flag_in = 0;  // Semaphore variant: the flag as the previous step left it
-  if constexpr (kDsm) {
-    // The shared word counts this step's end-stage adds from zero; the owner
-    // keeps the flag and counter of the previous step in registers, so the
-    // words obey the page's arithmetic: flag - counter = (flag_in + W + adds)
-    // - counter, i.e. W + adds - base with base = counter - flag_in.
-    if (tid == owner) st_shared(flag_sh, 0u);
-  }
+  // Semaphore variant: the owner keeps the flag and counter of the previous
+  // step in registers, so the words obey the page's arithmetic: flag -
+  // counter = (flag_in + W + adds) - counter, i.e. W + adds - base with
+  // base = counter - flag_in.
 
   // The first batch of this block's staging loads.  They read only the
   // caller's input, which no barrier guards, so they are issued before the
@@ -363,11 +375,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     // PullController start stage (unfenced): its W signals are the W blocks'
     // arrivals at the cluster barrier, which every block has passed once
     // this wait returns -- counted into the flag as W at write-back.  The
-    // owner's warp arrives with release, so the zeroed word is in place
-    // before any peer's add can reach it; the other warps arrive relaxed (a
-    // release arrival by every warp measured about 2 % slower).
+    // owner's warp arrived (with release) before the dependency wait; the
+    // other warps arrive relaxed here, after their first staging loads.
     __syncwarp();  // the cluster barrier instructions are warp-aligned
-    if (warp == r) cluster_arrive_release(); else cluster_arrive_relaxed();
+    if (warp != r) cluster_arrive_relaxed();
     __syncwarp();
     cluster_wait();
   } else if constexpr (kCluster) {
@@ -472,14 +483,21 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   }
   // 4. end barrier, fenced: every thread's staging precedes the release.
   __syncthreads();
+  // The cluster-launched variants count the block past the copy between their
+  // end-stage arrival and wait and look at the count's old value later, so
+  // the atomic's round trip overlaps the cluster barrier (and, in the cluster
+  // variant, the reduce) instead of holding warp 1 before the barrier:
+  // 3.43 against 3.56 us per step in the cluster variant (W = 8 [32, 4096],
+  // A/B in one process).  The Semaphore variant publishes right after the
+  // cluster barrier, before its end-stage check, so a block held in that
+  // check by a missing signal does not hold back `published` (the host
+  // watchdog reports a step published but not done).
+  uint32_t published_old = 0;
   if constexpr (kCluster) {
     // Release on arrive (after the block barrier: the whole block's staging),
     // acquire on wait; the published count runs between the two.
     cluster_arrive_release();
-    if (tid == 32u && atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
-      hdr->blocks[0] = 0u;
-      st_relaxed_gpu(&hdr->published, seq);
-    }
+    if (tid == 32u) published_old = atomicAdd(&hdr->blocks[0], 1u);
     __syncwarp();
     cluster_wait();
   } else if constexpr (kPad) {
@@ -520,13 +538,14 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       red_add_relaxed_cluster(cluster_peer_address(flag_sh, warp), 1u);
     __syncwarp();
     cluster_arrive_release();
-    if (tid == 32u && atomicAdd(&hdr->blocks[0], 1u) == total_blocks - 1u) {
+    if (tid == 32u) published_old = atomicAdd(&hdr->blocks[0], 1u);
+    __syncwarp();
+    cluster_wait();
+    if (tid == 32u && published_old == total_blocks - 1u) {
       // Last block past the copy publishes seq (only the host watchdog reads it).
       hdr->blocks[0] = 0u;
       st_relaxed_gpu(&hdr->published, seq);
     }
-    __syncwarp();
-    cluster_wait();
     if (tid == owner) {
       // flag - counter = (flag_in + W + adds) - (flag_in + base): the page's
       // unsigned test flag - counter >= 2W is adds - (base - W) >= 2W.
@@ -624,6 +643,14 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     pad_barrier<kFencedAll>(pad, B, uint32_t(W), b, r, tid, true, a.timeout_ns, &hdr->err, kPadSend,
                             kPadWait);
   } else if (tid == 32u) {
+    if constexpr (kCluster) {
+      // Last block past the copy publishes seq (only the host watchdog reads
+      // it); its count was taken at the end barrier.
+      if (published_old == total_blocks - 1u) {
+        hdr->blocks[0] = 0u;
+        st_relaxed_gpu(&hdr->published, seq);
+      }
+    }
     epoch[r * B + b] = (s_epoch + 1u) % 2u;  // PushController::exit
     // Staggered steps: the fence orders this block's read of T0 (before the
     // block barriers above) before its exit count, so the last block out,

@@ -256,9 +256,9 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
  *                       a bounded wait that waits only when a signal is
  *                       missing (the fault knob skips one, as in the flag
  *                       modes below).  The flag and counter are loaded from
- *                       the workspace at entry and written back at exit, so
- *                       the words follow the same arithmetic as in the global
- *                       form.  The hardware barrier's waits complete because
+ *                       the workspace at entry and written back after that
+ *                       check, so the words follow the same arithmetic as in
+ *                       the global form.  The hardware barrier's waits complete because
  *                       every thread arrives unconditionally.  Steps with
  *                       slots in host memory that stage in turn (see
  *                       arx_ctx_init_split) run in the global form
