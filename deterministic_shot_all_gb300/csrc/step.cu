@@ -41,8 +41,6 @@
 //    has finished reading the slots).
 //  * Semaphore, global: steps 2 and 4 with the flags in the workspace (as the
 //    page keeps them for peers on other GPUs), step 6 a relaxed pad barrier.
-//    Also used for host-slot steps that stage in turn (their waits cross
-//    clusters).
 //  * Pad: every barrier is triton_barrier.py's `blockwise_barrier` on the
 //    signal pad, in the page's three patterns -- Pattern 0 at the start
 //    (relaxed barrier, then block sync), Pattern 1 after staging (block sync,
@@ -282,7 +280,6 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   constexpr bool kDsm = kSync == kSyncSemaphore;    // clusters too; Semaphores in shared memory
   constexpr bool kSemGlobal = kSync == kSyncSemaphoreGlobal;
   constexpr bool kFencedAll = kSync == kSyncPadFenced;
-  static_assert(!(kStagger && kDsm), "host-slot steps stagger with the Semaphores in global memory");
   const uint32_t b = blockIdx.x, r = blockIdx.y;
   const uint32_t B = uint32_t(a.B);
   const uint32_t tid = threadIdx.x, warp = tid / 32u, lane = tid % 32u;
@@ -686,15 +683,16 @@ int blocks_per_sm(int dev, cudaError_t* err) {
     if (c > 0) return c;
   }
   int lo = 0;
-  const void* kernels[9] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, true>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncPad, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphoreGlobal, false>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphoreGlobal, true>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncPad, true>),
-                            reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, true>)};
+  const void* kernels[10] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, true>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, true>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, false>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, false>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphoreGlobal, false>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphoreGlobal, true>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncPad, true>),
+                             reinterpret_cast<const void*>(step_kernel<W, kSyncPadFenced, true>)};
   for (const void* k : kernels) {
     int b = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, 0);
@@ -759,16 +757,13 @@ cudaError_t launch_w(const StepCall& c, cudaStream_t stream) {
   cattr[1] = attr[1];
   switch (c.sync_mode) {
     case kSyncSemaphore:
-      if (st) {
-        // Staggered steps (slots in host memory) run the Semaphores in global
-        // memory: 18.5-18.8 us per step against 19.0 with the flags in
-        // shared memory (W = 8 [32, 4096], GB300).
-        err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphoreGlobal, true>, a);
-      } else {
-        cfg.attrs = cattr;
-        cfg.numAttrs = 2;
-        err = cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore, false>, a);
-      }
+      // Staggered steps (slots in host memory) too: 18.4 us per step
+      // against 18.9 with the Semaphores in global memory (W = 8
+      // [32, 4096], A/B in one process, GB300).
+      cfg.attrs = cattr;
+      cfg.numAttrs = 2;
+      err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore, true>, a)
+               : cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphore, false>, a);
       break;
     case kSyncSemaphoreGlobal:
       err = st ? cudaLaunchKernelEx(&cfg, step_kernel<W, kSyncSemaphoreGlobal, true>, a)
@@ -820,7 +815,8 @@ int cluster_capacity_w(cudaError_t* err) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int lo = 0;
-  const void* kernels[3] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+  const void* kernels[4] = {reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, false>),
+                            reinterpret_cast<const void*>(step_kernel<W, kSyncSemaphore, true>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, false>),
                             reinterpret_cast<const void*>(step_kernel<W, kSyncCluster, true>)};
   for (const void* k : kernels) {

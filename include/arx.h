@@ -258,11 +258,9 @@ arx_status arx_ctx_set_timeout(arx_ctx* ctx, uint64_t ns);
  *                       modes below).  The flag and counter are loaded from
  *                       the workspace at entry and written back after that
  *                       check, so the words follow the same arithmetic as in
- *                       the global form.  The hardware barrier's waits complete because
- *                       every thread arrives unconditionally.  Steps with
- *                       slots in host memory that stage in turn (see
- *                       arx_ctx_init_split) run in the global form
- *                       (ARX_SYNC_SEMAPHORE_GLOBAL), measured faster there.
+ *                       the global form.  The hardware barrier's waits
+ *                       complete because every thread arrives
+ *                       unconditionally.
  *  ARX_SYNC_SEMAPHORE_GLOBAL  the same barriers with the Semaphores in the
  *                       workspace (global memory), as the page keeps them for
  *                       peers on other GPUs: release adds and acquire polls
