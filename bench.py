@@ -134,8 +134,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+def stored_traffic(workload: str, n: int) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if taken on this
+    kernel source at this size."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as fh:
@@ -144,6 +145,8 @@ def stored_traffic(workload: str) -> float | None:
         return None
     e = rec.get(workload)
     if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    if e.get("n") is not None and int(e["n"]) != n:
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -523,7 +526,7 @@ def run_native(args) -> None:
     peak_note = "of measured" if peak else "of fallback"
     peak = float(peak) if peak else FALLBACK_HBM_GBS
     achieved = gbs(bytes_call, per_call)
-    traffic = stored_traffic(args.workload)
+    traffic = stored_traffic(args.workload, n)
     cpu = cpu1 = None
     if not args.no_cpu_baseline:
         import oracle
@@ -572,8 +575,9 @@ def reduce_kernel_name(W: int, n: int, alias: bool, sms: int = 152) -> str:
 
     Exact for the one-vector 8-byte form (128 threads per block while
     256-thread blocks would number fewer than the SMs, as at the decode-sized
-    workloads; 256 for W >= 5, or while one pass of a grid of sms x 8 blocks
-    covers the n / 4 vectors) and for the 16-byte form above 2^22 elements;
+    workloads; 256 for W = 5-7, or while one pass of a grid of sms x 8 blocks
+    covers the n / 4 vectors with 1/16 slack), for W = 8 past that pass (the
+    pipelined 16-byte form) and for the 16-byte form above 2^22 elements;
     W <= 4 messages between take a batched 8-byte form or the 16-byte one by
     the library's one-pass rule.
     """
@@ -582,14 +586,14 @@ def reduce_kernel_name(W: int, n: int, alias: bool, sms: int = 152) -> str:
         blocks256 = -(-(2 * (n // 8)) // 256)
         if blocks256 < sms:
             return f"reduce_half_kernel<{W}, 128, 1, {a}>"
-        if W >= 5 or blocks256 <= sms * 8:
+        if 5 <= W <= 7 or blocks256 * 16 <= sms * 8 * 17:
             return f"reduce_half_kernel<{W}, 256, 1, {a}>"
+        if W == 8:
+            return f"reduce_vec_kernel<8, 256, 1, 1, {a}>"
         return f"reduce_half_kernel<{W}, 256, U, {a}> (batched) or reduce_vec_kernel (one-pass rule)"
     if W <= 2:
         return f"reduce_vec_kernel<{W}, 128, 2, 1, {a}>"
-    if W <= 4:
-        return f"reduce_vec_kernel<{W}, 256, 1, 1, {a}>"
-    return f"reduce_vec_kernel<{W}, 256, 2, 0, {a}>"
+    return f"reduce_vec_kernel<{W}, 256, 1, 1, {a}>"
 
 
 def bandwidth_points(torch, arx, sp, dev, stream, l2) -> list:

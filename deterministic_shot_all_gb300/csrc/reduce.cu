@@ -21,8 +21,8 @@
 //    thread per iteration, all W*U loads issued before the first add
 //    (Little's law against HBM3e latency);
 //  * software pipelining (kPipe): the next iteration's loads are in flight
-//    while the current groups are summed and stored -- measured best for
-//    W <= 4 at large sizes;
+//    while the current groups are summed and stored -- measured best at
+//    every W once the body needs more than one pass of the grid;
 //  * programmatic dependent launch: the kernel waits on its stream
 //    predecessor (griddepcontrol.wait) before touching memory and lets its
 //    successor start launching at once, which hides most of the launch gap
@@ -348,7 +348,15 @@ cudaError_t launch_half(const VecArgs& a, int dev, int sms, bool force, bool* ta
 //  n <= 2^22: the 8-byte form, 128 threads per block while blocks of 256
 //             would number fewer than the SMs (W = 8 at 2^12 - 2^17 elements:
 //             2.6-7.3 % faster than 256; 64 threads gained less), else 256.
-//             W >= 5: one vector per slot per thread.
+//             W = 5-7: one vector per slot per thread.
+//             W = 8: one vector while one pass of the grid covers the body
+//             (+ 1/16), else the pipelined 16-byte form below: 0.97-1.03
+//             against 0.77-0.92 of the copy rate from 2^20.75 to 2^22 (a
+//             second pass of the 8-byte form waits for its first loads;
+//             the pipelined form keeps the next group's loads in flight).
+//             At W = 5-7 it won only at some of those sizes and lost at
+//             others (W = 7 at 2^20.5: 0.74 against 0.88), so they keep the
+//             one-vector form.
 //             W <= 4: one vector while one pass of the grid covers the
 //             body, else kHalfU<W> vectors while one pass covers it, else
 //             the 16-byte form below -- the batched form saves 5-20 % over
@@ -357,8 +365,9 @@ cudaError_t launch_half(const VecArgs& a, int dev, int sms, bool force, bool* ta
 //             threads load again only after their first loads returned, at
 //             the end of the burst).
 //  above:     16-byte groups -- W <= 2: 128 threads, U = 2, pipelined;
-//             W 3-4: 256 threads, U = 1, pipelined; W >= 5: 256 threads,
-//             U = 2 without pipelining (more loads in flight per thread).
+//             W >= 3: 256 threads, U = 1, pipelined (for W >= 5 it replaced
+//             U = 2 without pipelining: +3-10 % from 2^22.5 to 2^25, equal
+//             at 2^26, within 0.5 % at 2^27).
 constexpr size_t kHalfMaxElems = size_t(1) << 22;
 
 template <int W, bool kAlias>
@@ -371,7 +380,7 @@ cudaError_t launch_policy(const VecArgs& a, int dev, int sms, cudaStream_t strea
       // message (and its L2 prefetches) over twice as many SMs.
       return launch_half<W, 128, 1, kAlias>(a, dev, sms, true, &taken, stream);
     }
-    err = launch_half<W, 256, 1, kAlias>(a, dev, sms, W >= 5, &taken, stream);
+    err = launch_half<W, 256, 1, kAlias>(a, dev, sms, W >= 5 && W < 8, &taken, stream);
     if (err != cudaSuccess || taken) return err;
     if constexpr (kHalfU<W> > 1) {
       err = launch_half<W, 256, kHalfU<W>, kAlias>(a, dev, sms, false, &taken, stream);
@@ -384,10 +393,8 @@ cudaError_t launch_policy(const VecArgs& a, int dev, int sms, cudaStream_t strea
   }
   if constexpr (W <= 2) {
     return launch_vec<W, 128, 2, true, kAlias>(a, dev, sms, stream);
-  } else if constexpr (W <= 4) {
-    return launch_vec<W, 256, 1, true, kAlias>(a, dev, sms, stream);
   } else {
-    return launch_vec<W, 256, 2, false, kAlias>(a, dev, sms, stream);
+    return launch_vec<W, 256, 1, true, kAlias>(a, dev, sms, stream);
   }
 }
 
