@@ -86,12 +86,13 @@ def test_random_reduces_stay_in_bounds(checked):
     dev = torch.device("cuda:0")
     _violations(checked)
     rng = np.random.default_rng(5150)
-    sizes = [(1 << 22) - 3, (1 << 22) + 9, (1 << 23) + 5, (1 << 21) + 5]
+    sizes = [(1 << 22) - 3, (1 << 22) + 9, (1 << 23) + 5, (1 << 21) + 5, 1_400_003]
     for case in range(120):
         W = int(rng.integers(1, 9))
         if case % 10 == 0:
-            n = sizes[(case // 10) % 4]
+            n = sizes[(case // 10) % 5]
             W = 1 + (case // 10) % 4 if n == (1 << 21) + 5 else W  # the batched 8-byte form
+            W = 8 if n == 1_400_003 else W  # the pipelined 16-byte form past one 8-byte pass
         else:
             n = int(rng.integers(0, 5000))
         same = bool(rng.integers(0, 2))

@@ -153,6 +153,30 @@ def test_batched_8_byte_form(arx, dev, W, n, alias):
     assert not buf[row, 0].view(torch.int16).item() and not buf[row, 1 + n:].view(torch.int16).any()
 
 
+@pytest.mark.parametrize("W", [5, 7, 8])
+@pytest.mark.parametrize("n", [1_250_003, 1_400_003, (1 << 21) + 5, (1 << 22) - 1, (1 << 22) + 9, 9_000_011])
+@pytest.mark.parametrize("alias", [False, True])
+def test_pipelined_16_byte_form(arx, dev, W, n, alias):
+    # W = 8 takes the pipelined 16-byte form (one group per slot per thread,
+    # the next group's loads in flight while the current one is summed) once
+    # one pass of the one-vector 8-byte grid no longer covers the body (with
+    # 1/16 slack: on 152 SMs 1,250,003 elements stay in the 8-byte form,
+    # 1,400,003 leave it); W = 5-7 keep the 8-byte form, with a second pass,
+    # up to 2^22; above 2^22 every W >= 5 takes the pipelined form, several
+    # passes of it at 9,000,011.  Scalar head (pointers 2 bytes past a
+    # 16-byte boundary), ragged tail, in place or not; guard elements intact.
+    x = sp.partials(W, n, "normal", seed=n % 991 + 10 * W + alias)
+    want = oracle.reduce(list(sp.to_u16_numpy(x)), threads=oracle.default_threads())
+    buf = torch.zeros(W + 1, n + 16, dtype=torch.bfloat16, device=dev)
+    buf[:W, 1:1 + n] = x.to(dev)
+    slots = [buf[r, 1:1 + n] for r in range(W)]
+    row = W - 1 if alias else W
+    arx.arx_reduce(slots, buf[row, 1:1 + n])
+    torch.cuda.synchronize()
+    assert_bits_equal(buf[row, 1:1 + n].cpu().view(torch.int16).numpy(), want, f"W={W} n={n} alias={alias}")
+    assert not buf[row, 0].view(torch.int16).item() and not buf[row, 1 + n:].view(torch.int16).any()
+
+
 def test_alias_to_last_slot(arx, dev):
     x = sp.partials(5, 40000, "normal", seed=9)
     want = oracle.reduce(list(sp.to_u16_numpy(x)))
