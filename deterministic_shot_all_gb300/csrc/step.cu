@@ -123,9 +123,10 @@ struct Header {  // first bytes of the workspace (256 reserved)
   uint32_t blocks[2];  // blocks past staging / blocks finished
   uint32_t published;  // last staged seq
   uint32_t unused[27];
-  // Byte 128: the global timer value at which a staggered step's first block
-  // arrived (the groups' start times count from it); the step's last block
-  // out zeroes it, so it is zero between steps.
+  // Byte 128: the start of the last staggered step -- its seq in the high
+  // half, the low 32 bits of the global timer when its first block arrived
+  // in the low half (the groups' start times count from it); zero before
+  // the context's first staggered step.
   unsigned long long stagger_t0;
   uint32_t unused2[30];
 };
@@ -413,8 +414,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // Staggered staging (slots in host memory): the blocks form K groups by
   // chunk, and group g starts writing its slots at T0 + g * stagger_ns,
   // where T0 is the global timer when the step's first block got here
-  // (compare-and-swapped into the header) and stagger_ns is the time the
-  // link takes to write one group's staged bytes.  So the writes to host
+  // (compare-and-swapped into the header, tagged with the step's seq, so a
+  // block that finds its own step's tag takes that T0 and nothing has to
+  // clear the word afterwards) and stagger_ns is the time the link takes to
+  // write one group's staged bytes.  So the writes to host
   // memory go out at about the link's rate, group after group, and each
   // group's reads (after its end barrier) overlap the later groups' writes
   // on the full-duplex link.  A scheduling delay only -- the barriers order
@@ -422,17 +425,29 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
   // T0 asks for longer), and no block waits for another.  Measured (W = 8
   // [32, 4096], GB300): 18.5-18.8 us per step against 22.2 us when each
   // group waited for the previous one's count through L2 (about 1.1 us per
-  // hand-off, 16 hand-offs) and 23.5 us with every group at once.  Compiled
-  // only into the kernels of host-slot steps.
+  // hand-off, 16 hand-offs) and 23.5 us with every group at once; 18.17
+  // against 18.75 us with T0 untagged and zeroed by the last block out
+  // (two fences and a store on that block's exit path).  A tag left from
+  // 2^32 steps earlier would only cost one step its pacing: the start times
+  // compare in 32-bit modular time, so a stale T0 reads as long past.
+  // Compiled only into the kernels of host-slot steps.
   uint32_t K = 0, grp = 0;
   if constexpr (kStagger) {
     K = a.stagger;
     grp = b * K / B;
     if (tid == 0) {
       const unsigned long long now = global_timer_ns();
-      const unsigned long long old = atomicCAS(&hdr->stagger_t0, 0ull, now);
-      const unsigned long long target = (old ? old : now) + grp * a.stagger_ns;
-      for (uint64_t spins = 0; global_timer_ns() < target; ++spins) {
+      const unsigned long long mine = (static_cast<unsigned long long>(seq) << 32) | (now & 0xFFFFFFFFull);
+      unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(&hdr->stagger_t0);
+      if (static_cast<uint32_t>(cur >> 32) != seq) {
+        // Only blocks of this step write the word while it runs, so a failed
+        // swap returns the start another block of this step installed.
+        const unsigned long long old = atomicCAS(&hdr->stagger_t0, cur, mine);
+        cur = old == cur ? mine : old;
+      }
+      const uint32_t t0 = static_cast<uint32_t>(cur);
+      const uint32_t delay = static_cast<uint32_t>(grp * a.stagger_ns);
+      for (uint64_t spins = 0; static_cast<uint32_t>(global_timer_ns()) - t0 < delay; ++spins) {
         if (global_timer_ns() - now > a.timeout_ns || spins > spin_cap(a.timeout_ns)) {
           record_error(&hdr->err, kErrTimeout, kStaggerWait, r, b);
           break;
@@ -649,16 +664,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
       }
     }
     epoch[r * B + b] = (s_epoch + 1u) % 2u;  // PushController::exit
-    // Staggered steps: the fence orders this block's read of T0 (before the
-    // block barriers above) before its exit count, so the last block out,
-    // fenced again, zeroes T0 after every block has read it.
-    if constexpr (kStagger) __threadfence();
     if (atomicAdd(&hdr->blocks[1], 1u) == total_blocks - 1u) {  // last block out
       hdr->blocks[1] = 0u;
-      if constexpr (kStagger) {
-        __threadfence();
-        hdr->stagger_t0 = 0ull;
-      }
       st_relaxed_gpu(&hdr->seq, seq);
     }
   }

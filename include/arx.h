@@ -156,8 +156,10 @@ arx_status arx_reduce_host(const void* const* host_slots, int W, void* host_out,
  *   [0, 256)        header, uint32: seq (completed steps), err (device error
  *                   word, 0 = none), blocks[2] (publish / exit counters),
  *                   published (last staged seq); at byte 128 a uint64,
- *                   the start time of a staggered host-slot step (zero
- *                   between steps)
+ *                   the start of the last staggered host-slot step: its
+ *                   seq in the high half, the low 32 bits of its
+ *                   global-timer start in the low half (zero before the
+ *                   first)
  *   off_epoch       uint32 epoch[W][B]                    (PushController)
  *   off_sem         struct { uint32 flag, counter; } sem[W][B], 128-byte
  *                   stride                                (Semaphore)

@@ -103,6 +103,19 @@ class Ctx:
         self.ws[off: off + 4] = torch.tensor([value], dtype=torch.int64).view(torch.uint8)[:4].to(self.ws.device)
 
 
+def _assert_stagger_word(words, last_staggered_seq):
+    """Staggered staging's start word (header bytes 128-135): the seq of the
+    context's last staggered step in its high half (the low half is that
+    step's global-timer start), zero before the first; the rest of the
+    header's upper half zero."""
+    w = words["stagger"]
+    if last_staggered_seq:
+        assert w[1] == last_staggered_seq, (int(w[1]), last_staggered_seq)
+    else:
+        assert not w[:2].any()
+    assert not w[2:].any()
+
+
 def _stagger_groups(W, n, B):
     """Block groups of a host-slot step: about 128 KiB of staged data each, at
     most B; none below two (as include/arx.h describes)."""
@@ -167,11 +180,10 @@ def test_host_slot_steps_of_varying_size(arx, dev):
     # Slots in host memory: steps of 192 KiB of partials or more stage in
     # turn, in a number of block groups that follows each step's size; smaller
     # ones all at once.  Mixing them on one context must not matter: every
-    # output bit-exact, the staggered step's start time back to zero after
-    # every step.
+    # output bit-exact, the start word tagged with the last staggered step.
     W, max_n = 8, 131072
     c = Ctx(arx, dev, W, max_n, 0, "semaphore", "host")
-    staggered = 0
+    staggered = last = 0
     for s, n in enumerate((131072, 4096, 70001, 131072, 11, 65536)):
         for sync in SYNCS:
             arx.arx_ctx_set_sync(c.ctx, SYNCS.index(sync))
@@ -181,8 +193,10 @@ def test_host_slot_steps_of_varying_size(arx, dev):
             assert (st, err) == (arx.ARX_OK, 0)
             assert_bits_equal(out.cpu().view(torch.int16).numpy(), oracle.reduce(list(sp.to_u16_numpy(x))),
                               f"n={n} {sync}")
-            staggered += bool(_stagger_groups(W, n, c.B))
-            assert not c.words()["stagger"].any(), (n, sync, seq)
+            if _stagger_groups(W, n, c.B):
+                staggered += 1
+                last = seq
+            _assert_stagger_word(c.words(), last)
     assert staggered > 0
 
 
@@ -329,9 +343,9 @@ def test_protocol_words_follow_the_model(arx, dev, W, n, B, k, sync, slots):
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"step {s}")
         _compare_to_model(c.words(), st)
     assert (c.words()["flag"] == (2 * W * k if sync in SEM_SYNCS else 0)).all()
-    # Staggered staging's start time: zero between steps (the last block out
-    # of a staggered step clears it), host slots or not.
-    assert not c.words()["stagger"].any()
+    # Staggered staging's start word: tagged with the last step when the
+    # steps staged in turn (host slots), else never written.
+    _assert_stagger_word(c.words(), k if slots == "host" and _stagger_groups(W, n, c.B) else 0)
     for r in range(W):
         assert np.array_equal(c.slot(k & 1, r, n), hist[k - 1][r])
         if k >= 2:
@@ -586,7 +600,7 @@ def test_ten_thousand_steps_in_one_graph(arx, dev, graph_workload, sync, slots):
     assert (w["flag"] == flags).all() and (w["counter"] == w["flag"]).all()
     assert (w["epoch"] == steps % 2).all() and w["blocks"] == [0, 0]
     assert w["published"] == steps
-    assert not w["stagger"].any()
+    _assert_stagger_word(w, steps if slots == "host" and _stagger_groups(W8, N8, c.B) else 0)
     for r in range(W8):
         assert np.array_equal(c.slot(steps & 1, r, N8), last_two[steps - 1][r])
         assert np.array_equal(c.slot((steps - 1) & 1, r, N8), last_two[steps - 2][r])
