@@ -33,9 +33,9 @@
 //    flag through distributed shared memory, then the cluster barrier
 //    (release arrival, acquire wait) orders the staged slots and the adds;
 //    the owner then checks flag - counter >= 2W, bounded, which waits only
-//    if a signal is missing.  The flag and counter are loaded at entry and
-//    written back after that check, so the words in memory follow the same
-//    arithmetic.  No add is in flight after the end barrier, so no exit
+//    if a signal is missing.  The flag and counter are loaded at entry (by
+//    thread 0, with seq and the epoch) and written back after that check, so
+//    the words in memory follow the same arithmetic.  No add is in flight after the end barrier, so no exit
 //    barrier is needed; the kernel boundary stands in for Pattern 2 (the
 //    next kernel on the stream starts only after every block of this one
 //    has finished reading the slots).
@@ -106,7 +106,6 @@ enum SyncMode : int {
 
 // 16-byte vectors each thread loads before storing them while staging.
 constexpr int kStageBatch = 4;
-
 
 // Bytes of its input chunk a block prefetches into L2 before the dependency
 // wait: its first two staging batches.  Only for messages whose W inputs
@@ -538,14 +537,15 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
     // it passes at once unless a signal is missing (the fault knob), in
     // which case it waits, bounded, and reports ARX_ETIMEOUT -- and advances
     // the counter.  Measured (W = 8 [32, 4096], GB300, A/B of library builds
-    // in one process): 4.0 us per step with this form (a build without the
+    // in one process): 4.0 us per step with this end stage before the start
+    // stage's changes above, 3.56-3.60 us with them (a build without the
     // adds and the check, which cannot count a missing signal, was no
-    // faster); 4.4-4.5 us with the
-    // owner polling its flag for release adds and no hardware barrier after
-    // staging, 4.6 us with the adds issued after the arrival (the check then
-    // waits for them, and an exit barrier must keep them from landing in an
-    // exited block), 5.6 us with the flags in global memory; the cluster
-    // variant, with no flag traffic at all, 3.5 us.
+    // faster); 4.4-4.5 us with the owner polling its flag for release adds
+    // and no hardware barrier after staging, 4.6 us with the adds issued
+    // after the arrival (the check then waits for them, and an exit barrier
+    // must keep them from landing in an exited block), 5.6 us with the flags
+    // in global memory; the cluster variant, with no flag traffic at all,
+    // 3.4-3.5 us.
     if (lane == 0 && warp < uint32_t(W) && int(r) != a.fault_rank)
       red_add_relaxed_cluster(cluster_peer_address(flag_sh, warp), 1u);
     __syncwarp();
