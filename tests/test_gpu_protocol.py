@@ -378,6 +378,40 @@ def test_unsigned_wrap_of_seq_and_flags(arx, dev):
     assert w["seq"] == 1
 
 
+def test_unsigned_wrap_with_staggered_host_slots(arx, dev):
+    # The same wrap on a host-slot context whose steps stage in turn.  The
+    # step numbered 0 finds the never-written start word's tag (0) equal to
+    # its seq and takes that stale start, so its groups start at once; the
+    # steps numbered 1 and 2 install their own.  Every output bit-exact, the
+    # words as the model says, the start word tagged with the last step.
+    W, n = 8, 131072
+    c = Ctx(arx, dev, W, n, 0, "semaphore", "host")
+    B = c.B
+    assert _stagger_groups(W, n, B)
+    seq0, flag0 = M32, M32 - 5      # 2^32 - 1 steps done: the next is numbered 0
+    c.poke(0, seq0)
+    ctx = c.ctx
+    for i in range(W * B):
+        c.poke(ctx.off_sem + 128 * i, flag0)
+        c.poke(ctx.off_sem + 128 * i + 4, flag0)
+        c.poke(ctx.off_epoch + 4 * i, seq0 % 2)
+    st = model.State(W=W, B=B, seq=seq0)
+    st.epoch[:] = seq0 % 2
+    st.flag[:] = flag0
+    st.counter[:] = flag0
+    st.published = 0
+    for s in range(3):
+        x = sp.partials(W, n, "normal", seed=60 + s)
+        out = _step(arx, c, x, dev)
+        want = model.step(st, list(sp.to_u16_numpy(x)))
+        assert arx.arx_ctx_query(c.ctx)[0] == arx.ARX_OK
+        assert_bits_equal(out.cpu().view(torch.int16).numpy(), want, f"host-slot wrap step {s}")
+    w = c.words()
+    _compare_to_model(w, st)
+    assert w["seq"] == 2
+    _assert_stagger_word(w, 2)
+
+
 @pytest.mark.parametrize("sync,slots", [(m, "one") for m in FLAG_SYNCS] + [("semaphore", "host")])
 def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
     W, n = 4, 8192
