@@ -40,6 +40,9 @@ def checked(arx):
             ("arx_reduce", [ptrs, i32, vp, sz, vp], i32),
             ("arx_ctx_workspace_bytes", [i32, sz, i32], sz),
             ("arx_ctx_init", [ctxp, vp, sz, i32, sz, i32], i32),
+            ("arx_ctx_words_bytes", [i32, i32], sz),
+            ("arx_ctx_slots_bytes", [i32, sz], sz),
+            ("arx_ctx_init_split", [ctxp, vp, sz, vp, sz, i32, i32, sz, i32], i32),
             ("arx_ctx_set_sync", [ctxp, i32], i32),
             ("arx_step", [ctxp, ptrs, vp, sz, vp], i32),
             ("arx_bounds_violations", [ctypes.POINTER(ctypes.c_uint32), i32], i32),
@@ -124,9 +127,21 @@ def test_random_steps_stay_in_bounds(checked, arx):
         B = int(rng.integers(0, 8))
         mode = int(rng.integers(0, 5))   # every barrier variant, the cluster ones included
         in_off, out_off = int(rng.integers(0, 8)), int(rng.integers(0, 8))
-        ws = torch.zeros(checked.arx_ctx_workspace_bytes(W, n, B), dtype=torch.uint8, device=dev)
         ctx = arx.arx_ctx()
-        assert checked.arx_ctx_init(ctypes.byref(ctx), ws.data_ptr(), ws.numel(), W, n, B) == 0
+        if case % 12 == 0:
+            # Slots in page-locked host memory, 2 MiB partials: the steps stage
+            # in turn (the staggered kernels), in the default mode, the
+            # cluster mode and a random one.
+            mode = {0: 0, 12: 3}.get(case, mode)
+            B = max(B, 2)
+            ws = torch.zeros(checked.arx_ctx_words_bytes(W, B), dtype=torch.uint8, device=dev)
+            slots = torch.empty(checked.arx_ctx_slots_bytes(W, n), dtype=torch.uint8).pin_memory()
+            assert checked.arx_ctx_init_split(ctypes.byref(ctx), ws.data_ptr(), ws.numel(), slots.data_ptr(),
+                                              slots.numel(), arx.ARX_SLOTS_HOST, W, n, B) == 0, \
+                checked.arx_last_error()
+        else:
+            ws = torch.zeros(checked.arx_ctx_workspace_bytes(W, n, B), dtype=torch.uint8, device=dev)
+            assert checked.arx_ctx_init(ctypes.byref(ctx), ws.data_ptr(), ws.numel(), W, n, B) == 0
         assert checked.arx_ctx_set_sync(ctypes.byref(ctx), mode) == 0
         for s in range(2):
             x = sp.partials(W, n, "normal", seed=40_000 + 2 * case + s)

@@ -412,10 +412,14 @@ def test_unsigned_wrap_with_staggered_host_slots(arx, dev):
     _assert_stagger_word(w, 2)
 
 
-@pytest.mark.parametrize("sync,slots", [(m, "one") for m in FLAG_SYNCS] + [("semaphore", "host")])
-def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots):
-    W, n = 4, 8192
+@pytest.mark.parametrize("sync,slots,n", [(m, "one", 8192) for m in FLAG_SYNCS]
+                         + [("semaphore", "host", 8192), ("semaphore", "host", 65536)])
+def test_timeout_is_reported_and_context_recovers(arx, dev, sync, slots, n):
+    # n = 65536 on host slots: 512 KiB of partials, so the step stages in turn
+    # (two block groups at B = 2) and the staggered kernel's end wait expires.
+    W = 4
     c = Ctx(arx, dev, W, n, 2, sync, slots)
+    assert bool(_stagger_groups(W, n, c.B)) == (slots == "host" and n == 65536)
     x = sp.partials(W, n, "normal", seed=8)
     _step(arx, c, x, dev)
     assert arx.arx_ctx_query(c.ctx)[:2] == (arx.ARX_OK, 1)
