@@ -23,7 +23,7 @@ struct ReduceCall {
   size_t n;
   int W;
   bool out_aliases_slot;  // out equals one slot pointer
-  bool prefetch_l2;       // buffers are device memory: the kernel may prefetch them into L2
+  bool prefetch_l2;       // the kernel may prefetch its slots into L2 before the dependency wait
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif

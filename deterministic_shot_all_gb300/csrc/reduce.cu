@@ -28,10 +28,10 @@
 //    successor start launching at once, which hides most of the launch gap
 //    between back-to-back calls;
 //  * before that wait, one thread per block issues bulk L2 prefetches of the
-//    block's first chunk of every slot (device buffers only), so the next
-//    call's DRAM latency overlaps the current call -- a prefetch consumes no
-//    data, so a predecessor that writes those partials stays correct (the
-//    loads come after the wait and read through L2).  W = 8 [32, 4096]:
+//    block's first chunk of every slot (device or page-locked host buffers),
+//    so the next call's DRAM or link latency overlaps the current call -- a
+//    prefetch consumes no data, so a predecessor that writes those partials
+//    stays correct (the loads come after the wait and read through L2).  W = 8 [32, 4096]:
 //    1.60 -> 1.42 us per call; W = 2 at 2^23 elements: 8.76 -> 7.66 us.
 // The launch policy (threads, U, kPipe per W and size) comes from a measured
 // sweep of these shapes on GB300.
@@ -56,7 +56,7 @@ struct VecArgs {
   uint16_t* out;
   size_t n;        // elements
   size_t head;     // scalar elements before the first 16-byte boundary
-  int prefetch_l2; // device-memory buffers: warm L2 before the dependency wait
+  int prefetch_l2; // warm L2 with the slots before the dependency wait
 #ifdef ARX_BOUNDS_CHECK
   uint32_t* bounds_counter;
 #endif
