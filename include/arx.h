@@ -98,7 +98,10 @@ arx_status arx_reduce(const void* const* slots, int W, void* out, size_t n, void
  * kernel reads the partials and writes the sum in host memory itself, over
  * GB300's coherent CPU-GPU link, as arx.cu does on GB10 ("pinned host buffers
  * are GPU buffers").  One kernel, no copies; dev_staging is not used and may
- * be NULL.
+ * be NULL.  As in arx_reduce, the kernel may prefetch the partials into L2
+ * before the previous kernel on the stream has finished (a hint: the data it
+ * sums are read after that kernel's writes; the CPU must not write the
+ * buffers while the call is in flight).
  * Staged form -- otherwise: one cudaMemcpyAsync per slot into dev_staging,
  * the reduce in place over staged slot 0, one cudaMemcpyAsync back (copies
  * from and to pageable memory synchronise with the host).
