@@ -12,7 +12,10 @@ the oracle, so a stale line from the previous call would show:
 * ``arx_reduce_host`` (direct form) with a separate host output, and in place
   (the output one of the partials);
 * ``arx_step`` whose inputs are page-locked host buffers rewritten by the
-  CPU, with the slot banks in device memory and in page-locked host memory.
+  CPU, with the slot banks in device memory and in page-locked host memory;
+* chained calls, each reading the previous call's output, on device and on
+  page-locked host buffers (the L2 prefetch issued before the dependency
+  wait touches the buffer the predecessor is still writing).
 """
 
 import pytest
@@ -105,3 +108,53 @@ def test_step_rereads_rewritten_host_inputs(arx, dev, slots_where):
         assert_bits_equal(out.cpu().view(torch.int16).numpy(), wants[(i + 1) % len(xs)], f"replayed step {i}")
     st, seq, err = arx.arx_ctx_query(ctx, stream=s)
     assert (st, seq, err) == (arx.ARX_OK, 2 * CALLS, 0)
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_chained_calls_read_their_predecessors_output(arx, dev, where):
+    # Each call's output is the next call's first partial, enqueued back to
+    # back on one stream (and replayed from one captured graph).  The reduce
+    # prefetches its partials into L2 before it waits for its predecessor,
+    # so here the prefetch touches a buffer the predecessor is still
+    # writing; the loads after the wait must see the finished sum.  Device
+    # buffers through arx_reduce, page-locked host buffers through
+    # arx_reduce_host.
+    W, n, steps = 4, 131072 + 3, 24
+    x = sp.partials(W, n, "normal", seed=33_000 + (where == "host"))
+    u = list(sp.to_u16_numpy(x))
+    wants, first = [], u[0]
+    for _ in range(steps):
+        first = oracle.reduce([first] + u[1:], threads=4)
+        wants.append(first)
+    if where == "device":
+        parts = x.to(dev)
+        outs = torch.zeros(steps, n, dtype=torch.bfloat16, device=dev)
+    else:
+        parts = x.clone().pin_memory()
+        outs = torch.zeros(steps, n, dtype=torch.bfloat16).pin_memory()
+    s = torch.cuda.Stream()
+
+    def run():
+        for k in range(steps):
+            slots = [outs[k - 1] if k else parts[0]] + [parts[r] for r in range(1, W)]
+            if where == "device":
+                arx.arx_reduce(slots, outs[k], stream=s)
+            else:
+                arx.arx_reduce_host(slots, outs[k], stream=s)
+
+    run()
+    s.synchronize()
+    for k in range(steps):
+        assert_bits_equal(outs[k].cpu().view(torch.int16).numpy(), wants[k], f"{where} eager call {k}")
+    g = torch.cuda.CUDAGraph()
+    outs.zero_() if where == "device" else outs.fill_(0)
+    with torch.cuda.graph(g, stream=s):
+        run()
+    for rep in range(3):
+        outs.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        for k in range(steps):
+            assert_bits_equal(outs[k].cpu().view(torch.int16).numpy(), wants[k], f"{where} replay {rep} call {k}")
